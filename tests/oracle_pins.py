@@ -1,0 +1,374 @@
+"""Pins for the oracle: checks against facts that do not come from the oracle itself.
+
+Each ``*_pin_failures`` function takes the oracle functions as arguments and
+returns the list of pins that fail (empty = all hold).  The pin tests call them
+with the real oracle; the mutant tests call them with deliberately broken
+copies to show that a plausible mistake (dropped term, wrong sign, transposed
+operand, wrong axis, wrong order) is caught.
+
+Sources of truth used here: hand-worked examples under tests/golden, closed
+forms of special cases, explicit-matrix brute force, scalar-loop re-derivations
+and invariants of the gated delta rule, brute-force subset search for top-k.
+"""
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rng(seed=1234):
+    return np.random.default_rng(seed)
+
+
+# --------------------------------------------------------------------------------------
+# KDA step
+# --------------------------------------------------------------------------------------
+
+def kda_pin_failures(step):
+    fails = []
+    A = np.asarray
+
+    # 1. hand-worked examples (exact, dyadic)
+    for ex in _load("kda_worked_examples.json")["examples"]:
+        S_t, o = step(A(ex["S"], float), A(ex["q"], float), A(ex["k"], float),
+                      A(ex["v"], float), A(ex["alpha"], float), np.float64(ex["beta"]))
+        if np.shape(S_t) != np.shape(ex["S_t"]) or not np.array_equal(S_t, A(ex["S_t"], float)):
+            fails.append(f"golden S_t {ex['name']}")
+        if np.shape(o) != np.shape(ex["o"]) or not np.array_equal(o, A(ex["o"], float)):
+            fails.append(f"golden o {ex['name']}")
+
+    rng = _rng()
+    dk, dv = 5, 7
+    S = rng.standard_normal((dk, dv))
+    q, k, al = rng.standard_normal(dk), rng.standard_normal(dk), rng.uniform(0.1, 0.9, dk)
+    v = rng.standard_normal(dv)
+
+    # 2. beta = 0, alpha = 1: state unchanged, o = S^T q (scalar loops)
+    S_t, o = step(S, q, k, v, np.ones(dk), np.float64(0.0))
+    if not np.array_equal(S_t, S):
+        fails.append("beta=0 alpha=1 keeps S")
+    o_ref = [sum(S[i, j] * q[i] for i in range(dk)) for j in range(dv)]
+    if not np.allclose(o, o_ref, rtol=1e-13, atol=1e-13):
+        fails.append("beta=0 alpha=1 output S^T q")
+
+    # 3. beta = 0: S_t = diag(alpha) S, i.e. row i scaled by alpha_i
+    S_t, _ = step(S, q, k, v, al, np.float64(0.0))
+    ref = np.array([[al[i] * S[i, j] for j in range(dv)] for i in range(dk)])
+    if not np.array_equal(S_t, ref):
+        fails.append("beta=0 gives diag(alpha) S")
+
+    # 4. S = 0, alpha = 1, beta = 1, k = e_i: S_t = e_i v^T, o = q_i v
+    i0 = 3
+    e = np.zeros(dk); e[i0] = 1.0
+    S_t, o = step(np.zeros((dk, dv)), q, e, v, np.ones(dk), np.float64(1.0))
+    ref = np.zeros((dk, dv)); ref[i0] = v
+    if not np.array_equal(S_t, ref):
+        fails.append("write into empty state")
+    if not np.array_equal(o, q[i0] * v):
+        fails.append("read after write into empty state")
+
+    # 5. delta retrieval: beta ||k||^2 = 1 => k^T S_t = v^T for any alpha, S
+    c = 2.0
+    S_t, _ = step(S, q, c * e, v, al, np.float64(1.0 / (c * c)))
+    if not np.array_equal(S_t[i0], v / c):
+        fails.append("delta retrieval (axis key, exact)")
+    kd = rng.standard_normal(dk)
+    S_t, _ = step(S, q, kd, v, al, np.float64(1.0 / float(kd @ kd)))
+    if not np.allclose(kd @ S_t, v, rtol=1e-12, atol=1e-12):
+        fails.append("delta retrieval (dense key)")
+
+    # 6. brute force with the explicit d_k x d_k transition matrix, d <= 8
+    for (a, b) in [(1, 1), (3, 2), (8, 8), (4, 6)]:
+        Sx = rng.standard_normal((a, b))
+        qx, kx, alx = rng.standard_normal(a), rng.standard_normal(a), rng.uniform(0.05, 0.95, a)
+        vx, bx = rng.standard_normal(b), rng.uniform(0.05, 1.0)
+        Tm = (np.eye(a) - bx * np.outer(kx, kx)) @ np.diag(alx)
+        S_ref = Tm @ Sx + bx * np.outer(kx, vx)
+        S_t, o = step(Sx, qx, kx, vx, alx, np.float64(bx))
+        if not (np.allclose(S_t, S_ref, rtol=1e-12, atol=1e-12)
+                and np.allclose(o, S_ref.T @ qx, rtol=1e-12, atol=1e-12)):
+            fails.append(f"explicit-matrix brute force {a}x{b}")
+
+    # 7. scalar-loop re-derivation through u = k^T diag(alpha) S (column by column)
+    be = 0.37
+    S_t, o = step(S, q, k, v, al, np.float64(be))
+    ok = True
+    for j in range(dv):
+        u = sum(k[i] * al[i] * S[i, j] for i in range(dk))
+        col = [al[i] * S[i, j] + be * k[i] * (v[j] - u) for i in range(dk)]
+        oj = sum(col[i] * q[i] for i in range(dk))
+        ok &= np.allclose(S_t[:, j], col, rtol=1e-12, atol=1e-12) and math.isclose(o[j], oj, rel_tol=1e-12, abs_tol=1e-12)
+    if not ok:
+        fails.append("column-wise scalar re-derivation")
+
+    # 8. column separability: updating a column subset alone equals the full update
+    cols = [0, 2, 5]
+    S_sub, o_sub = step(S[:, cols], q, k, v[cols], al, np.float64(be))
+    if not (np.allclose(S_sub, S_t[:, cols], rtol=1e-14, atol=1e-14)
+            and np.allclose(o_sub, o[cols], rtol=1e-14, atol=1e-14)):
+        fails.append("column separability")
+
+    # 9. o is linear in q
+    q2 = rng.standard_normal(dk)
+    _, o1 = step(S, q, k, v, al, np.float64(be))
+    _, o2 = step(S, q2, k, v, al, np.float64(be))
+    _, o12 = step(S, q + 2.0 * q2, k, v, al, np.float64(be))
+    if not np.allclose(o12, o1 + 2.0 * o2, rtol=1e-12, atol=1e-12):
+        fails.append("o linear in q")
+
+    # 10. leading batch axes behave like independent calls
+    Sb = rng.standard_normal((2, 3, dk, dv))
+    qb, kb, alb = (rng.standard_normal((2, 3, dk)), rng.standard_normal((2, 3, dk)),
+                   rng.uniform(0.1, 0.9, (2, 3, dk)))
+    vb, bb = rng.standard_normal((2, 3, dv)), rng.uniform(0, 1, (2, 3))
+    S_tb, ob = step(Sb, qb, kb, vb, alb, bb)
+    for b in range(2):
+        for h in range(3):
+            s1, o1 = step(Sb[b, h], qb[b, h], kb[b, h], vb[b, h], alb[b, h], bb[b, h])
+            if not (np.allclose(S_tb[b, h], s1, rtol=1e-14, atol=1e-14)
+                    and np.allclose(ob[b, h], o1, rtol=1e-14, atol=1e-14)):
+                fails.append("batched axes")
+                break
+    return sorted(set(fails))
+
+
+# --------------------------------------------------------------------------------------
+# speculative window: verify / accept / replay
+# --------------------------------------------------------------------------------------
+
+def spec_pin_failures(step, verify, accept, replay):
+    fails = []
+    for ex in _load("accept_worked_examples.json")["examples"]:
+        a, c = accept(np.array([ex["draft"]]), np.array([ex["target"]]), np.array([ex["committed"]]))
+        if int(a[0]) != ex["accepted"] or int(c[0]) != ex["committed_after"]:
+            fails.append(f"accept golden {ex['draft']}")
+
+    # brute force over every match pattern for T = 5
+    T = 5
+    for pattern in itertools.product([0, 1], repeat=T):
+        draft = np.arange(10, 10 + T)[None]
+        target = np.where(np.array(pattern)[None] == 1, draft, draft + 100)
+        expect = next((t for t in range(T) if pattern[t] == 0), T)
+        a, c = accept(draft, target, np.array([3]))
+        if int(a[0]) != expect or int(c[0]) != 3 + expect:
+            fails.append("accept brute force")
+            break
+
+    # the hand-worked two-step chain from the golden file
+    exs = _load("kda_worked_examples.json")["examples"]
+    e1, e3 = exs[0], exs[2]
+    q = np.array([[[e1["q"]], [e3["q"]]]], float)      # [B=1, T=2, H=1, d]
+    k = np.array([[[e1["k"]], [e3["k"]]]], float)
+    v = np.array([[[e1["v"]], [e3["v"]]]], float)
+    al = np.array([[[e1["alpha"]], [e3["alpha"]]]], float)
+    be = np.array([[[e1["beta"]], [e3["beta"]]]], float)
+    S_c = np.array([[e1["S"]]], float)                 # [B=1, H=1, 2, 2]
+    S_c_before = S_c.copy()
+    o = verify(S_c, q, k, v, al, be)
+    if not (np.array_equal(o[0, 0, 0], e1["o"]) and np.array_equal(o[0, 1, 0], e3["o"])):
+        fails.append("verify golden chain")
+    if not np.array_equal(S_c, S_c_before):
+        fails.append("verify must not modify the committed state")
+    for a, expect in [(0, e1["S"]), (1, e1["S_t"]), (2, e3["S_t"])]:
+        S_new = replay(S_c, q, k, v, al, be, np.array([a]))
+        if not np.array_equal(S_new[0, 0], np.array(expect, float)):
+            fails.append(f"replay golden a={a}")
+
+    # random window: replay(a) equals a sequential steps; verify(T) outputs equal steps
+    rng = _rng(7)
+    B, T, H, dk, dv = 3, 4, 2, 4, 3
+    S_c = rng.standard_normal((B, H, dk, dv))
+    q, k = rng.standard_normal((B, T, H, dk)), rng.standard_normal((B, T, H, dk))
+    v = rng.standard_normal((B, T, H, dv))
+    al, be = rng.uniform(0.1, 0.9, (B, T, H, dk)), rng.uniform(0, 1, (B, T, H))
+    o = verify(S_c, q, k, v, al, be)
+    acc = np.array([0, 2, 4])
+    S_new = replay(S_c, q, k, v, al, be, acc)
+    for b in range(B):
+        S_all = S_c[b].copy()          # every drafted token (what verify scores)
+        S_acc = S_c[b].copy()          # accepted tokens only (what replay commits)
+        for t in range(T):
+            S_all, ot = step(S_all, q[b, t], k[b, t], v[b, t], al[b, t], be[b, t])
+            if not np.allclose(ot, o[b, t], rtol=1e-13, atol=1e-13):
+                fails.append("verify equals sequential steps")
+            if t < acc[b]:
+                S_acc, _ = step(S_acc, q[b, t], k[b, t], v[b, t], al[b, t], be[b, t])
+        if not np.allclose(S_acc, S_new[b], rtol=1e-13, atol=1e-13):
+            fails.append("replay equals sequential accepted steps")
+    if not np.array_equal(S_new[0], S_c[0]):
+        fails.append("replay with nothing accepted keeps the committed state")
+    return sorted(set(fails))
+
+
+# --------------------------------------------------------------------------------------
+# router, experts, RMSNorm, linear, bf16 rounding
+# --------------------------------------------------------------------------------------
+
+def _sig(z):
+    return 1.0 / (1.0 + math.exp(-z))
+
+
+def moe_pin_failures(route_topk, moe_forward, swiglu_expert, rmsnorm, linear, round_bf16, silu):
+    fails = []
+
+    # bf16 rounding table (hand-worked from the bit layout)
+    for c in _load("bf16_rounding.json")["cases"]:
+        if float(round_bf16(np.array([c["x"]]))[0]) != c["bf16"]:
+            fails.append(f"bf16 rounding {c['x']}")
+
+    # SiLU special values
+    if not (float(silu(np.array([0.0]))[0]) == 0.0
+            and math.isclose(float(silu(np.array([2.0]))[0]), 2.0 * _sig(2.0), rel_tol=1e-15)
+            and abs(float(silu(np.array([-40.0]))[0])) < 1e-15
+            and math.isclose(float(silu(np.array([40.0]))[0]), 40.0, rel_tol=1e-15)):
+        fails.append("silu special values")
+
+    # RMSNorm: constant vector and a hand case
+    cval, eps = 3.0, 1e-6
+    y = rmsnorm(np.full((1, 4), cval), np.array([1.0, 2.0, -1.0, 0.5]), eps)
+    if not np.allclose(y[0], np.array([1.0, 2.0, -1.0, 0.5]) * cval / math.sqrt(cval * cval + eps), rtol=1e-15):
+        fails.append("rmsnorm constant vector")
+    y = rmsnorm(np.array([[3.0, 4.0]]), np.array([1.0, 1.0]), 0.0)
+    if not np.allclose(y[0], np.array([3.0, 4.0]) / math.sqrt(12.5), rtol=1e-15):
+        fails.append("rmsnorm hand case")
+
+    # linear: x W^T hand case
+    y = linear(np.array([[1.0, 2.0, 3.0]]), np.array([[1.0, 0.0, 0.0], [0.0, 1.0, -1.0]]))
+    if not np.array_equal(y, np.array([[1.0, -1.0]])):
+        fails.append("linear hand case")
+
+    # hand-worked 3-expert router + SwiGLU case (Hd=2, I=1), closed forms with exp
+    x = np.array([[2.0, 3.0]])
+    W_r = np.array([[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]])   # logits 2, 3, 5
+    Wg = np.array([[[1.0, 0.0]], [[0.0, 1.0]], [[-1.0, -1.0]]])
+    Wu = np.array([[[0.0, 2.0]], [[1.0, 1.0]], [[1.0, 0.0]]])
+    Wd = np.array([[[1.0], [-1.0]], [[2.0], [0.0]], [[0.0], [1.0]]])
+    idx, w, logits = route_topk(x, W_r, 2)
+    s3, s5 = _sig(3.0), _sig(5.0)
+    if list(idx[0]) != [2, 1]:
+        fails.append("router hand case order")
+    if not np.allclose(w[0], [s5 / (s3 + s5), s3 / (s3 + s5)], rtol=1e-14):
+        fails.append("router hand case weights")
+    if not np.allclose(logits[0], [2.0, 3.0, 5.0], rtol=0, atol=0):
+        fails.append("router logits")
+    # expert 2: g=-5, u=2 -> h = -10 sig(-5), y = [0, h]; expert 1: g=3,u=5 -> h = 15 sig(3), y = [2h, 0]
+    # shared: g=5, u=-1 -> h = -5 sig(5) -> [h, h]; residual [1, -1]
+    shared = [(np.array([[1.0, 1.0]]), np.array([[1.0, -1.0]]), np.array([[1.0], [1.0]]))]
+    w1, w2 = s3 / (s3 + s5), s5 / (s3 + s5)
+    h_sh = -5.0 * s5
+    expect = np.array([w1 * 30.0 * s3 + h_sh + 1.0, w2 * (-10.0 * _sig(-5.0)) + h_sh - 1.0])
+    y = moe_forward(x, idx, w, (Wg, Wu, Wd), shared, residual=np.array([[1.0, -1.0]]))
+    if not np.allclose(y[0], expect, rtol=1e-14, atol=1e-14):
+        fails.append("moe hand case")
+
+    # tie-break: identical router rows -> lower index first
+    W_t = np.array([[1.0, 1.0], [0.5, 0.5], [1.0, 1.0], [0.0, 0.0]])
+    idx, _, _ = route_topk(np.array([[1.0, 1.0]]), W_t, 3)
+    if list(idx[0]) != [0, 2, 1]:
+        fails.append("router tie-break")
+
+    # brute force: the chosen set maximises the score sum over all k-subsets
+    rng = _rng(11)
+    E, Hd, kk = 9, 6, 3
+    xs = rng.standard_normal((5, Hd))
+    Wr = rng.standard_normal((E, Hd))
+    idx, w, _ = route_topk(xs, Wr, kk)
+    sc = 1.0 / (1.0 + np.exp(-(xs @ Wr.T)))
+    for m in range(5):
+        best = max(itertools.combinations(range(E), kk), key=lambda s: sum(sc[m, list(s)]))
+        if set(idx[m]) != set(best):
+            fails.append("router brute force set")
+        if not all(sc[m, idx[m, j]] > sc[m, idx[m, j + 1]] for j in range(kk - 1)):
+            fails.append("router descending order")
+        if not math.isclose(float(np.sum(w[m])), 1.0, rel_tol=0, abs_tol=1e-15):
+            fails.append("router weights sum to one")
+
+    # E = 1, k = 1: a dense SwiGLU MLP, written as scalar loops
+    Hd, I = 4, 3
+    g1, u1, d1 = rng.standard_normal((I, Hd)), rng.standard_normal((I, Hd)), rng.standard_normal((Hd, I))
+    xt = rng.standard_normal((2, Hd))
+    y = moe_forward(xt, np.zeros((2, 1), int), np.ones((2, 1)), (g1[None], u1[None], d1[None]))
+    for m in range(2):
+        hh = []
+        for i in range(I):
+            gi = sum(g1[i, j] * xt[m, j] for j in range(Hd))
+            ui = sum(u1[i, j] * xt[m, j] for j in range(Hd))
+            hh.append(gi / (1.0 + math.exp(-gi)) * ui)
+        ref = [sum(d1[r, i] * hh[i] for i in range(I)) for r in range(Hd)]
+        if not np.allclose(y[m], ref, rtol=1e-12, atol=1e-12):
+            fails.append("dense SwiGLU special case")
+
+    # zero down projection -> zero output; permuting experts with their weights -> unchanged
+    E = 5
+    Wg, Wu, Wd = rng.standard_normal((E, I, Hd)), rng.standard_normal((E, I, Hd)), rng.standard_normal((E, Hd, I))
+    idx = np.array([[1, 4], [0, 3]])
+    w = np.array([[0.7, 0.3], [0.4, 0.6]])
+    if not np.array_equal(moe_forward(xt, idx, w, (Wg, Wu, np.zeros_like(Wd))), np.zeros((2, Hd))):
+        fails.append("zero down projection")
+    perm = np.array([3, 0, 4, 1, 2])           # expert e is stored at slot perm[e]
+    inv = np.argsort(perm)
+    y1 = moe_forward(xt, idx, w, (Wg, Wu, Wd))
+    y2 = moe_forward(xt, perm[idx], w, (Wg[inv], Wu[inv], Wd[inv]))
+    if not np.allclose(y1, y2, rtol=1e-14, atol=1e-14):
+        fails.append("expert permutation invariance")
+    if not np.allclose(moe_forward(xt, idx[:, ::-1], w[:, ::-1], (Wg, Wu, Wd)), y1, rtol=1e-13, atol=1e-13):
+        fails.append("slot order invariance")
+    return sorted(set(fails))
+
+
+# --------------------------------------------------------------------------------------
+# layer pieces
+# --------------------------------------------------------------------------------------
+
+def layer_pin_failures(qkvg_epilogue, decode_layer, step, rmsnorm, round_bf16):
+    fails = []
+    # epilogue special values: g = 0 -> alpha = exp(-ln 2) = 1/2; beta logit 0 -> 1/2;
+    # q = [3, 4] -> [0.6, 0.8] -> bf16 [0.6015625, 0.80078125] (see golden bf16 table)
+    H, dk, dv = 1, 2, 2
+    z = np.array([[3.0, 4.0, 0.0, -2.0, 1.0, -1.0, 0.0, 0.0, 0.0]])
+    q, k, v, al, be = qkvg_epilogue(z, H, dk, dv)
+    if not np.array_equal(q[0, 0], [0.6015625, 0.80078125]):
+        fails.append("q normalisation")
+    if not np.array_equal(k[0, 0], [0.0, -1.0]):
+        fails.append("k normalisation")
+    if not np.array_equal(v[0, 0], [1.0, -1.0]):
+        fails.append("v passthrough")
+    if not (np.array_equal(al[0, 0], [0.5, 0.5]) and float(be[0, 0]) == 0.5):
+        fails.append("alpha / beta at zero")
+    # large gate -> alpha ~ e^-g (strong decay); very negative gate -> alpha -> 1
+    z2 = np.array([[1.0, 0.0, 1.0, 0.0, 1.0, 0.0, 20.0, -20.0, 0.0]])
+    _, _, _, al2, _ = qkvg_epilogue(z2, H, dk, dv)
+    if not (math.isclose(float(al2[0, 0, 0]), math.exp(-20.0), rel_tol=1e-6)
+            and math.isclose(float(al2[0, 0, 1]), 1.0, rel_tol=1e-8)):
+        fails.append("alpha limits")
+
+    # composition: zero o-proj and zero experts -> y == x; state equals one KDA step
+    rng = _rng(3)
+    M, H, dk, dv, Hd, E, I, kk = 2, 2, 4, 4, 8, 4, 3, 2
+    x = round_bf16(rng.standard_normal((M, Hd)))
+    S = rng.standard_normal((M, H, dk, dv))
+    p = dict(H=H, dk=dk, dv=dv, top_k=kk, eps=1e-6,
+             gamma_attn=round_bf16(1 + 0.1 * rng.standard_normal(Hd)),
+             gamma_moe=round_bf16(1 + 0.1 * rng.standard_normal(Hd)),
+             W_qkvgb=round_bf16(0.3 * rng.standard_normal((3 * H * dk + H * dv + H, Hd))),
+             W_o=np.zeros((Hd, H * dv)), W_r=rng.standard_normal((E, Hd)))
+    experts = (rng.standard_normal((E, I, Hd)), rng.standard_normal((E, I, Hd)), np.zeros((E, Hd, I)))
+    y, S_new, aux = decode_layer(x, S, p, experts)
+    if not np.array_equal(y, x):
+        fails.append("layer residual path")
+    x1 = round_bf16(rmsnorm(x, p["gamma_attn"], 1e-6))
+    qq, kq, vq, aq, bq = qkvg_epilogue(x1 @ p["W_qkvgb"].T, H, dk, dv)
+    S_ref, o_ref = step(S, qq, kq, vq, aq, bq)
+    if not (np.allclose(S_new, S_ref, rtol=1e-14, atol=1e-14) and np.allclose(aux["o"], o_ref, rtol=1e-14, atol=1e-14)):
+        fails.append("layer KDA composition")
+    return sorted(set(fails))
