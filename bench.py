@@ -1,0 +1,650 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark: one hybrid decode layer (KDA + routed MoE) plus one speculative
+window (verify, accept, replay) per step, through the C-ABI library.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload of one step (synthetic, seeded):
+  * hybrid decode layer, batch 64: RMSNorm(7168) -> q/k/v/gate/beta projection
+    (7168 -> 32x128 x4 + 32) -> KDA step on 64 fp32 states [32,128,128] -> output
+    projection 4096 -> 7168 + residual -> RMSNorm -> router (256 experts, top-8, sigmoid)
+    -> routed SwiGLU experts (intermediate 2048, ~22.5 GB of bf16 weights) + 1 shared
+    expert + residual, with the side-stream L2 prefetch;
+  * speculative window on 16 other sequences, 4 drafted tokens each: verify (no state
+    write), accepted-length bookkeeping (accepted length uniform in 0..4), replay of the
+    accepted prefix from the committed state.
+The metric is achieved HBM bandwidth over the step: algorithmic bytes (weights streamed,
+states read and written, activations; scratch traffic not credited) / step time.  The
+step's working set (~20 GB) is far larger than the 129 MB L2, so every step reads cold.
+
+The one JSON line also carries: µs per step, a roofline entry for the dominant kernel
+(routed-expert gate/up streaming, timed live with CUDA events on its launching stream),
+an end-to-end number through host buffers, clocks sampled during the timed region, the
+number of library kernel launches, batch sweeps, and the fp64 oracle timed on the host
+cores as the CPU baseline.  `--impl reference` times that oracle alone as the reference
+arm on a bounded sample of the same workload.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode µs/step and achieved HBM GB/s (KDA + MoE) vs GB300 peak at batch 1–64"
+CFG = dict(M=64, Hd=7168, H=32, d=128, E=256, k=8, I=2048, n_shared=1, eps=1e-6,
+           spec_B=16, spec_T=4)
+ROTATE = 4  # distinct input batches cycled through the timed steps
+
+
+# ----------------------------------------------------------------------------- bytes
+
+def layer_bytes(M, U, c=CFG):
+    """Algorithmic HBM bytes of one decode layer over M sequences with U active experts."""
+    Hd, H, d, E, k, I, ns = c["Hd"], c["H"], c["d"], c["E"], c["k"], c["I"], c["n_shared"]
+    Nq = 4 * H * d + H
+    b = dict(
+        rmsnorm=2 * (2 * M * Hd * 2 + Hd * 2),
+        qkvg=Nq * Hd * 2 + M * Hd * 2 + 3 * M * H * d * 2 + M * H * d * 4 + M * H * 4,
+        kda=M * H * (8 * d * d + 3 * d * 2 + d * 4 + 4 + d * 2),
+        oproj=Hd * H * d * 2 + M * H * d * 2 + 2 * M * Hd * 2,
+        router=E * Hd * 2 + M * Hd * 2 + M * k * 8,
+        experts=(U + ns) * 3 * I * Hd * 2 + 3 * M * Hd * 2,
+    )
+    return b
+
+
+def spec_bytes(B, T, accepted, c=CFG):
+    H, d = c["H"], c["d"]
+    tok = 3 * d * 2 + d * 4 + 4
+    return dict(verify=B * H * (4 * d * d + T * (tok + 4 * d)),
+                accept=2 * B * T * 4 + 3 * B * 4,
+                replay=sum(H * (8 * d * d + int(a) * tok) for a in accepted if a > 0))
+
+
+def gateup_bytes(M, U, c=CFG):
+    """Algorithmic bytes of one routed+shared gate/up launch."""
+    P = M * (c["k"] + c["n_shared"])
+    return (U + c["n_shared"]) * 2 * c["I"] * c["Hd"] * 2 + M * c["Hd"] * 2 + P * c["I"] * 2
+
+
+def kda_bytes(B, c=CFG, o_bytes=4):
+    H, d = c["H"], c["d"]
+    return B * H * (8 * d * d + 3 * d * 2 + d * 4 + 4 + d * o_bytes)
+
+
+# ----------------------------------------------------------------------------- host helpers
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while measuring."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu, self.proc, self.path = gpu_index, None, None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.gpu}.csv")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.5)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["unsampled"], samples=0)
+        time.sleep(0.3)
+        self.proc.terminate()
+        self.proc.wait()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            n += 1
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(smax) if smax else None, reasons=sorted(reasons), samples=n)
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_over_ranks(elapsed_s, nbytes, world):
+    """(max elapsed over ranks, total bytes over ranks); identity on one rank."""
+    if world <= 1:
+        return elapsed_s, nbytes
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    b = torch.tensor([float(nbytes)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class Workload:
+    """Device-resident weights, states, rotating inputs and workspaces of one step."""
+
+    def __init__(self, dev, rank, prefetch=True):
+        import torch
+        from hybrid_linear_attention_gated_gb300 import hla, inputs
+        self.torch, self.hla, self.inputs, self.dev = torch, hla, inputs, dev
+        c = CFG
+        seed = 100 * rank
+        self.w = inputs.moe_weights(c["E"], c["Hd"], c["I"], c["n_shared"],
+                                    inputs.generator(seed + 3, dev), device=dev)
+        self.w.update(inputs.layer_weights(c["Hd"], c["H"], c["d"], c["d"],
+                                           inputs.generator(seed + 4, dev), device=dev))
+        self.L = hla.make_layer(c["Hd"], c["H"], c["d"], c["d"], c["E"], c["k"], c["I"],
+                                c["n_shared"], c["eps"], self.w)
+        M, H, d = c["M"], c["H"], c["d"]
+        g = inputs.generator(seed + 5, dev)
+        self.S = self.warm_states(M, g)
+        self.S_spec = self.warm_states(c["spec_B"], g)
+        self.x = [inputs.activations(M, c["Hd"], g, dev) for _ in range(ROTATE)]
+        B, T = c["spec_B"], c["spec_T"]
+        self.win, self.ids = [], []
+        for _ in range(ROTATE):
+            self.win.append(inputs.kda_inputs((B, T), H, d, d, g, dev))
+            dr, tg, a = inputs.accept_ids(B, T, g, dev)
+            self.ids.append((dr, tg, a.cpu().numpy()))
+        self.y = torch.empty(M, c["Hd"], dtype=torch.bfloat16, device=dev)
+        self.o_spec = torch.empty(B, T, H, d, device=dev)
+        self.acc = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.com = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.ws_bytes = hla.hla_decode_layer_workspace_size(self.L, M)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.side = torch.cuda.Stream(device=dev) if prefetch else 0
+
+    def warm_states(self, B, g):
+        """States after 256 prior updates from zero, produced by the decode kernel itself."""
+        torch, hla, inputs = self.torch, self.hla, self.inputs
+        H, d = CFG["H"], CFG["d"]
+        S = torch.zeros(B, H, d, d, device=self.dev)
+        o = torch.empty(B, H, d, device=self.dev)
+        for _ in range(256):
+            u = inputs.kda_inputs((B,), H, d, d, g, self.dev)
+            hla.kda_decode_step(B, H, d, d, S, None, u["q"], u["k"], u["v"], u["alpha"], u["beta"], o)
+        return S
+
+    def step(self, i, x=None, win=None, ids=None):
+        hla, c = self.hla, CFG
+        r = i % ROTATE
+        x = self.x[r] if x is None else x
+        win = self.win[r] if win is None else win
+        dr, tg = (self.ids[r][0], self.ids[r][1]) if ids is None else ids
+        B, T, H, d = c["spec_B"], c["spec_T"], c["H"], c["d"]
+        hla.hla_decode_layer(self.L, c["M"], x, self.S, None, self.y, self.ws, self.ws_bytes,
+                             prefetch_stream=self.side)
+        hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, self.S_spec, None, win["q"],
+                                   win["k"], win["v"], win["alpha"], win["beta"], None, self.o_spec)
+        hla.spec_accept_prefix(B, T, dr, tg, self.acc, self.com)
+        hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, self.S_spec, None, win["q"],
+                                   win["k"], win["v"], win["alpha"], win["beta"], self.acc, None)
+
+    def active_experts(self):
+        torch = self.torch
+        ip, _ = self.hla.hla_decode_layer_routing(self.L, CFG["M"], self.ws)
+        idx = torch.empty(CFG["M"] * CFG["k"], dtype=torch.int32, device=self.dev)
+        # copy from the workspace address into a tensor
+        src = self.ws[ip - self.ws.data_ptr(): ip - self.ws.data_ptr() + idx.numel() * 4]
+        idx.view(torch.uint8).copy_(src)
+        return int(torch.unique(idx).numel())
+
+
+def time_steps(torch, fn, steps, world):
+    barrier(world)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(steps):
+        fn(i)
+    e1.record(st)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / 1e3
+
+
+def graph_time(torch, fn, iters, reps=3):
+    """Capture `iters` calls of fn(i) in one CUDA graph; median replay time per call (s)."""
+    fn(0)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(iters):
+                fn(i)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1) / 1e3 / iters)
+    del g
+    return statistics.median(out)
+
+
+def kda_sweep(torch, hla, inputs, dev, peak):
+    """KDA decode step alone at B in {1,2,8,32,64}: states rotated over a 512 MB pool (> 3x L2)."""
+    H, d = CFG["H"], CFG["d"]
+    pool_slots = 512 * 2 ** 20 // (H * d * d * 4)
+    pool = torch.randn(pool_slots, H, d, d, device=dev).mul_(0.05)
+    res = []
+    for B in (1, 2, 8, 32, 64):
+        iters = max(8, min(200, pool_slots // B))
+        g = inputs.generator(7000 + B, dev)
+        u = inputs.kda_inputs((B,), H, d, d, g, dev)
+        o = torch.empty(B, H, d, device=dev)
+        idxs = [torch.arange(i * B, (i + 1) * B, dtype=torch.int32, device=dev) % pool_slots
+                for i in range(iters)]
+
+        def fn(i):
+            hla.kda_decode_step(B, H, d, d, pool, idxs[i], u["q"], u["k"], u["v"], u["alpha"],
+                                u["beta"], o)
+        t = graph_time(torch, fn, iters)
+        gbs = kda_bytes(B) / t / 1e9
+        res.append(dict(batch=B, us=round(t * 1e6, 2), gbs=round(gbs, 1), frac=round(gbs / peak, 3),
+                        variant=hla.hla_last_variant()))
+    del pool
+    return res
+
+
+def moe_sweep(torch, hla, inputs, wl, dev, peak):
+    """Router + experts alone at M in {1,2,8,32,64} (the weights are ~22.5 GB: always cold)."""
+    c = CFG
+    res = []
+    for M in (1, 2, 8, 32, 64):
+        g = inputs.generator(8000 + M, dev)
+        xs = [inputs.activations(M, c["Hd"], g, dev) for _ in range(ROTATE)]
+        idx = torch.empty(M, c["k"], dtype=torch.int32, device=dev)
+        wt = torch.empty(M, c["k"], device=dev)
+        rb = hla.moe_route_topk_workspace_size(M, c["Hd"], c["E"])
+        rws = torch.empty(max(rb, 256), dtype=torch.uint8, device=dev)
+        nb = hla.moe_expert_forward_workspace_size(M, c["Hd"], c["I"], c["E"], c["k"], c["n_shared"])
+        mws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        y = torch.empty(M, c["Hd"], dtype=torch.bfloat16, device=dev)
+        w = wl.w
+        us = []
+        for r in range(ROTATE):
+            hla.moe_route_topk(M, c["Hd"], c["E"], c["k"], xs[r], w["W_r"], idx, wt, None, rws, rb)
+            us.append(int(torch.unique(idx).numel()))
+
+        def fn(i):
+            x = xs[i % ROTATE]
+            hla.moe_route_topk(M, c["Hd"], c["E"], c["k"], x, w["W_r"], idx, wt, None, rws, rb)
+            hla.moe_expert_forward(M, c["Hd"], c["I"], c["E"], c["k"], c["n_shared"], x, idx, wt,
+                                   w["W_gate"], w["W_up"], w["W_down"], w["Ws_gate"], w["Ws_up"],
+                                   w["Ws_down"], None, y, mws, nb)
+        t = graph_time(torch, fn, 4 * ROTATE)
+        U = statistics.mean(us)
+        nbytes = layer_bytes(M, U)["router"] + layer_bytes(M, U)["experts"]
+        gbs = nbytes / t / 1e9
+        res.append(dict(tokens=M, active_experts=U, us=round(t * 1e6, 1), gbs=round(gbs, 1),
+                        frac=round(gbs / peak, 3), variant=hla.hla_last_variant()))
+    return res
+
+
+def layer_sweep(torch, hla, inputs, wl, dev, peak):
+    c = CFG
+    res = []
+    for M in (1, 8, 64):
+        g = inputs.generator(9000 + M, dev)
+        xs = [inputs.activations(M, c["Hd"], g, dev) for _ in range(ROTATE)]
+        S = wl.S[:M].clone()
+        y = torch.empty(M, c["Hd"], dtype=torch.bfloat16, device=dev)
+        nb = hla.hla_decode_layer_workspace_size(wl.L, M)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+
+        def fn(i):
+            hla.hla_decode_layer(wl.L, M, xs[i % ROTATE], S, None, y, ws, nb, prefetch_stream=wl.side)
+        t = graph_time(torch, fn, 4 * ROTATE)
+        ip, _ = hla.hla_decode_layer_routing(wl.L, M, ws)
+        off = ip - ws.data_ptr()
+        U = int(torch.unique(ws[off:off + M * c["k"] * 4].view(torch.int32)).numel())
+        nbytes = sum(layer_bytes(M, U).values())
+        gbs = nbytes / t / 1e9
+        res.append(dict(batch=M, active_experts=U, us=round(t * 1e6, 1), gbs=round(gbs, 1),
+                        frac=round(gbs / peak, 3)))
+    return res
+
+
+def traffic_entry(kernel):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel sources are unchanged."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    import hashlib
+    h = hashlib.sha256()
+    for rel in t["sources"]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return t if h.hexdigest() == t["sources_sha256"] else None
+
+
+def cpu_baseline(wl, n_seq=4):
+    """The fp64 oracle, as it stands, on a bounded sample of the step (host cores)."""
+    import oracle
+    c = CFG
+    f = lambda t: t.detach().cpu().double().numpy()  # noqa: E731
+    p = dict(H=c["H"], dk=c["d"], dv=c["d"], top_k=c["k"], eps=c["eps"],
+             gamma_attn=f(wl.w["gamma_attn"]), gamma_moe=f(wl.w["gamma_moe"]),
+             W_qkvgb=f(wl.w["W_qkvgb"]), W_o=f(wl.w["W_o"]), W_r=f(wl.w["W_r"]))
+    x = f(wl.x[0][:n_seq])
+    S = f(wl.S[:n_seq])
+    cache = {}
+
+    def experts(e):
+        if e not in cache:
+            cache[e] = (f(wl.w["W_gate"][e]), f(wl.w["W_up"][e]), f(wl.w["W_down"][e]))
+        return cache[e]
+    shared = [(f(wl.w["Ws_gate"][0]), f(wl.w["Ws_up"][0]), f(wl.w["Ws_down"][0]))]
+    win = {k: f(v[:2]) for k, v in wl.win[0].items()}
+    S_spec = f(wl.S_spec[:2])
+    a = wl.ids[0][2][:2]
+
+    def sample():
+        used = set()
+        for m in range(n_seq):
+            _, _, aux = oracle.layer.decode_layer(x[m:m + 1], S[m:m + 1], p, experts, shared)
+            used.update(int(e) for e in aux["topk_idx"][0])
+        oracle.kda.spec_verify(S_spec, win["q"], win["k"], win["v"], win["alpha"], win["beta"])
+        oracle.kda.spec_replay(S_spec, win["q"], win["k"], win["v"], win["alpha"], win["beta"], a)
+        return used
+    sample()  # untimed: brings the sampled experts' weights to the host in fp64
+    t0 = time.perf_counter()
+    used = sample()
+    dt = time.perf_counter() - t0
+    nbytes = sum(layer_bytes(n_seq, len(used)).values()) + sum(spec_bytes(2, c["spec_T"], a).values())
+    return dict(value=round(nbytes / dt / 1e9, 4), unit="GB/s", cores=len(os.sched_getaffinity(0)),
+                kind="oracle", seconds=round(dt, 2),
+                sample=f"decode layer for {n_seq} of the 64 sequences (one at a time) + speculative "
+                       f"window for 2 of the 16 sequences, fp64 numpy oracle with the sampled "
+                       f"weights already on the host in fp64; bytes credited as for that sample")
+
+
+def run_ours(args):
+    import torch
+    from hybrid_linear_attention_gated_gb300 import build, hla, inputs
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build.build()
+    hla.load()
+    peak, peak_kind = peaks()
+    wl = Workload(dev, rank, prefetch=not args.no_prefetch)
+    c = CFG
+    for i in range(args.warmup):
+        wl.step(i)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    hla.hla_trace_enable("moe_gateup", args.steps)
+    n0 = hla.hla_launch_count()
+    elapsed = time_steps(torch, wl.step, args.steps, world)
+    launches = hla.hla_launch_count() - n0
+    gu_ms = hla.hla_trace_read(args.steps)
+    hla.hla_trace_enable(None, 0)
+
+    # active experts of the routed steps (routing depends on the evolving state: sample a few)
+    Us = []
+    for i in range(ROTATE):
+        wl.step(i)
+        torch.cuda.synchronize()
+        Us.append(wl.active_experts())
+    U = statistics.mean(Us)
+    per_step = layer_bytes(c["M"], U)
+    accepted = [wl.ids[i % ROTATE][2] for i in range(args.steps)]
+    spec_total = sum(sum(spec_bytes(c["spec_B"], c["spec_T"], a).values()) for a in accepted)
+    local_bytes = sum(per_step.values()) * args.steps + spec_total
+    t_max, all_bytes = reduce_over_ranks(elapsed, local_bytes, world)
+
+    # end to end through host buffers: pinned host inputs in, results out, every step
+    xh = [t.cpu().pin_memory() for t in wl.x]
+    winh = [{k: v.cpu().pin_memory() for k, v in w.items()} for w in wl.win]
+    idsh = [(d.cpu().pin_memory(), t.cpu().pin_memory()) for d, t, _ in wl.ids]
+    xd = torch.empty_like(wl.x[0])
+    wind = {k: torch.empty_like(v) for k, v in wl.win[0].items()}
+    dd, td = torch.empty_like(wl.ids[0][0]), torch.empty_like(wl.ids[0][1])
+    yh = torch.empty(wl.y.shape, dtype=wl.y.dtype).pin_memory()
+    oh = torch.empty(wl.o_spec.shape).pin_memory()
+    ah = torch.empty(wl.acc.shape, dtype=wl.acc.dtype).pin_memory()
+    h2d = xh[0].numel() * 2 + sum(v.numel() * v.element_size() for v in winh[0].values()) + \
+        2 * idsh[0][0].numel() * 4
+    d2h = yh.numel() * 2 + oh.numel() * 4 + ah.numel() * 4
+
+    def e2e_step(i):
+        r = i % ROTATE
+        xd.copy_(xh[r], non_blocking=True)
+        for k2, v in winh[r].items():
+            wind[k2].copy_(v, non_blocking=True)
+        dd.copy_(idsh[r][0], non_blocking=True)
+        td.copy_(idsh[r][1], non_blocking=True)
+        wl.step(i, x=xd, win=wind, ids=(dd, td))
+        yh.copy_(wl.y, non_blocking=True)
+        oh.copy_(wl.o_spec, non_blocking=True)
+        ah.copy_(wl.acc, non_blocking=True)
+    for i in range(2):
+        e2e_step(i)
+    e2e_elapsed = time_steps(torch, e2e_step, args.steps, world)
+    e2e_max, _ = reduce_over_ranks(e2e_elapsed, 0, world)
+
+    sweeps = {}
+    if not args.no_sweep and rank == 0:
+        sweeps["kda_decode"] = kda_sweep(torch, hla, inputs, dev, peak)
+        sweeps["moe"] = moe_sweep(torch, hla, inputs, wl, dev, peak)
+        sweeps["layer"] = layer_sweep(torch, hla, inputs, wl, dev, peak)
+    clocks = sampler.stop()
+
+    if rank != 0:
+        return
+    value = all_bytes / t_max / 1e9
+    gu_avg_s = statistics.mean(gu_ms) / 1e3 if gu_ms else None
+    gu_b = gateup_bytes(c["M"], U)
+    achieved = gu_b / gu_avg_s / 1e9 if gu_avg_s else None
+    tr = traffic_entry("moe_gateup_kernel")
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_max / args.steps * 1e3, 4),
+        "us_per_step": round(t_max / args.steps * 1e6, 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 weights/activations, fp32 KDA state and accumulation",
+        "data": "synthetic (seeded; random-init weights of the layer's shapes)",
+        "config": {
+            "workload": "hybrid decode layer at batch 64 (hidden 7168; KDA 32 heads x 128, fp32 "
+                        "state; 256 routed experts top-8 + 1 shared, intermediate 2048; L2 prefetch "
+                        "on a side stream) + speculative window B=16, T=4 (verify, accept, replay)",
+            "batch": c["M"], "spec_batch": c["spec_B"], "draft_len": c["spec_T"],
+            "active_experts_mean": U, "active_experts_samples": Us,
+            "bytes_per_step": round(local_bytes / args.steps),
+            "l2": "working set ~20 GB per step >> 129 MB L2 (inputs larger than L2; no flush)",
+            "parallelism": f"replicas x{world} (no collective on the data path)",
+            "launch": "eager launches on torch's current stream; prefetch on a second stream",
+        },
+        "breakdown_bytes_per_step": {**{k: v for k, v in per_step.items()},
+                                     **{"spec_" + k: v for k, v in spec_bytes(
+                                         c["spec_B"], c["spec_T"], wl.ids[0][2]).items()}},
+        "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "clock_samples": clocks["samples"],
+        "e2e": {"value": round(all_bytes / e2e_max / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_step": round(e2e_max / args.steps * 1e6, 1)},
+        "gpu_launches": int(launches),
+        "roofline": {
+            "kernel": "moe_gateup_kernel (routed + shared expert gate/up weight streaming)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1) if achieved else None,
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs copy bandwidth)" if peak_kind == "measured" else peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 3) if achieved else None,
+            "traffic": tr["bytes_per_launch"] if tr else None,
+            "algorithmic_bytes_per_launch": gu_b,
+            "avg_launch_us": round(gu_avg_s * 1e6, 1) if gu_avg_s else None,
+            "launches_timed": len(gu_ms),
+        },
+        "sweeps": sweeps,
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(out))
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The fp64 oracle on the host cores, each step a bounded sample of the workload:
+    the decode layer for one of the 64 sequences and the speculative window for one of
+    the 16 sequences."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    import oracle
+    from hybrid_linear_attention_gated_gb300 import inputs
+    c = CFG
+    f = lambda t: t.double().numpy()  # noqa: E731
+    g = inputs.generator(11)
+    lw = inputs.layer_weights(c["Hd"], c["H"], c["d"], c["d"], g)
+    W_r = inputs.weight((c["E"], c["Hd"]), g)
+    p = dict(H=c["H"], dk=c["d"], dv=c["d"], top_k=c["k"], eps=c["eps"],
+             gamma_attn=f(lw["gamma_attn"]), gamma_moe=f(lw["gamma_moe"]),
+             W_qkvgb=f(lw["W_qkvgb"]), W_o=f(lw["W_o"]), W_r=f(W_r))
+    cache = {}
+
+    def experts(e):  # each expert's weights drawn on first use from its own seed
+        if e not in cache:
+            ge = inputs.generator(3_000_000 + int(e))
+            cache[e] = tuple(f(inputs.weight(s, ge)) for s in
+                             ((c["I"], c["Hd"]), (c["I"], c["Hd"]), (c["Hd"], c["I"])))
+        return cache[e]
+    gs = inputs.generator(12)
+    shared = [tuple(f(inputs.weight(s, gs)) for s in
+                    ((c["I"], c["Hd"]), (c["I"], c["Hd"]), (c["Hd"], c["I"])))]
+    H, d, T = c["H"], c["d"], c["spec_T"]
+    u = inputs.warm_update_inputs(256, 2 * H, d, d, inputs.generator(13))
+    pool = oracle.kda.warm_state((2 * H, d, d), *(f(u[k]) for k in ("q", "k", "v", "alpha", "beta")))
+    S = pool[:H][None]
+    S_spec = pool[H:][None]
+    xs = [inputs.activations(1, c["Hd"], inputs.generator(20 + i)) for i in range(ROTATE)]
+    wins = [{k: f(v) for k, v in inputs.kda_inputs((1, T), H, d, d, inputs.generator(30 + i)).items()}
+            for i in range(ROTATE)]
+    accs = [inputs.accept_ids(1, T, inputs.generator(40 + i))[2].numpy() for i in range(ROTATE)]
+    for r in range(ROTATE):  # convert every expert the sample will touch before timing
+        oracle.layer.decode_layer(f(xs[r]), S, p, experts, shared)
+
+    def one(i):
+        r = i % ROTATE
+        _, _, aux = oracle.layer.decode_layer(f(xs[r]), S, p, experts, shared)
+        w = wins[r]
+        oracle.kda.spec_verify(S_spec, w["q"], w["k"], w["v"], w["alpha"], w["beta"])
+        oracle.kda.spec_replay(S_spec, w["q"], w["k"], w["v"], w["alpha"], w["beta"], accs[r])
+        U = len(set(int(e) for e in aux["topk_idx"][0]))
+        return sum(layer_bytes(1, U).values()) + sum(spec_bytes(1, T, accs[r]).values())
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    nbytes = sum(one(i) for i in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    cores = len(os.sched_getaffinity(0))
+    sample = ("per step: the decode layer for 1 of the 64 sequences and the speculative window "
+              "for 1 of the 16 sequences, fp64 numpy oracle; bytes credited as for that sample")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": "bounded sample of: hybrid decode layer batch 64 + speculative "
+                               "window B=16, T=4", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+    del np, torch
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefetch", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,418 @@
+// Skinny projections (split-K), the KDA input projection with its epilogue, RMSNorm,
+// the sigmoid top-k router and the L2 prefetch kernel.
+//
+// "Hyper-optimizing Kimi K3 in vLLM", Part 1 sec. 1: projections at decode batch
+// sizes are skinny products; the pages use small-matrix kernels at batch 1-2 and
+// split-K (K divided over more CTAs, then reduced) above.  Here every projection
+// runs on the warp-level streaming tile (stream_mma.cuh) and the split count is
+// chosen from the problem size so that enough 16-row x K-slice items exist to keep
+// every SM streaming; the second pass sums the fp32 partials in increasing slice
+// order, so results are deterministic.
+#include <cstdlib>
+
+#include "common.cuh"
+#include "stream_mma.cuh"
+
+namespace hla {
+
+int dense_auto_split(int M, int N, int K);   // shared with the layer executor
+int router_split(int M, int Hd, int E);
+
+namespace {
+
+constexpr int kDenseThreads = 128;  // 4 warps, one item per warp
+
+struct DenseParams {
+    const uint16_t *W;
+    const uint16_t *x;
+    int M, N, K;
+    int split, ntg;
+    float *part;               // [split][M][N] partials, or nullptr for the direct epilogue
+    void *y;                   // direct epilogue output [M][N]
+    int y_bf16;
+    const uint16_t *residual;  // direct epilogue residual [M][N] or nullptr
+};
+
+template <int NT, int UNROLL>
+__global__ void __launch_bounds__(kDenseThreads) dense_stream_kernel(const DenseParams p) {
+    const int item = (blockIdx.x * kDenseThreads + threadIdx.x) >> 5;
+    const int nrb = (p.N + 15) >> 4;
+    if (item >= nrb * p.split * p.ntg) return;  // whole warp leaves together
+    const int tg = item % p.ntg;
+    const int rest = item / p.ntg;
+    const int ks = rest % p.split;
+    const int rb = rest / p.split;
+    const int g = (threadIdx.x & 31) >> 2;
+
+    const uint16_t *wg[1] = {p.W + (size_t)min(rb * 16 + g, p.N - 1) * p.K};
+    const uint16_t *wg8[1] = {p.W + (size_t)min(rb * 16 + g + 8, p.N - 1) * p.K};
+    const uint16_t *xr[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+        xr[nt] = p.x + (size_t)min(tg * 8 * NT + nt * 8 + g, p.M - 1) * p.K;
+    int kb, ke;
+    k_slice(p.K, p.split, ks, kb, ke);
+
+    float acc[1][NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[0][nt][e] = 0.f;
+    warp_stream_tile<1, NT, UNROLL>(wg, wg8, xr, kb, ke, acc);
+
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = rb * 16 + acc_row(e);
+            const int m = tg * 8 * NT + acc_tok(nt, e);
+            if (r >= p.N || m >= p.M) continue;
+            const size_t o = (size_t)m * p.N + r;
+            if (p.part) {
+                p.part[(size_t)ks * p.M * p.N + o] = acc[0][nt][e];
+            } else {
+                float v = acc[0][nt][e];
+                if (p.residual) v = __fadd_rn(v, bf16_bits_to_float(p.residual[o]));
+                if (p.y_bf16)
+                    reinterpret_cast<uint16_t *>(p.y)[o] = float_to_bf16_bits(v);
+                else
+                    reinterpret_cast<float *>(p.y)[o] = v;
+            }
+        }
+    }
+}
+
+// y = sum over slices in increasing order (+ residual)
+__global__ void splitk_reduce_kernel(const float *__restrict__ part, int split, int M, int N,
+                                     const uint16_t *__restrict__ residual, void *y, int y_bf16) {
+    const size_t total = (size_t)M * N;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        float v = part[i];
+        for (int s = 1; s < split; ++s) v = __fadd_rn(v, part[(size_t)s * total + i]);
+        if (residual) v = __fadd_rn(v, bf16_bits_to_float(residual[i]));
+        if (y_bf16)
+            reinterpret_cast<uint16_t *>(y)[i] = float_to_bf16_bits(v);
+        else
+            reinterpret_cast<float *>(y)[i] = v;
+    }
+}
+
+// Fixed-order block sum (all threads get the result).  blockDim.x is a multiple of 32.
+__device__ float block_sum(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    float s = red[0];
+    for (int i = 1; i < nw; ++i) s = __fadd_rn(s, red[i]);
+    return s;
+}
+
+// q/k/v/gate/beta epilogue: one CTA of d threads per (token, head).
+__global__ void qkvg_epilogue_kernel(const float *__restrict__ part, int split, int M, int H, int d,
+                                     uint16_t *q, uint16_t *k, uint16_t *v, float *alpha,
+                                     float *beta) {
+    __shared__ float red[32];
+    const int m = blockIdx.x / H, h = blockIdx.x % H, i = threadIdx.x;
+    const int Nq = 4 * H * d + H;
+    const size_t plane = (size_t)M * Nq;
+    const float *row = part + (size_t)m * Nq;
+    auto sum = [&](int c) {
+        float s = row[c];
+        for (int sl = 1; sl < split; ++sl) s = __fadd_rn(s, row[(size_t)sl * plane + c]);
+        return s;
+    };
+    const int Hd_ = H * d;
+    const float zq = sum(h * d + i);
+    const float zk = sum(Hd_ + h * d + i);
+    const float zv = sum(2 * Hd_ + h * d + i);
+    const float zg = sum(3 * Hd_ + h * d + i);
+    const float ssq = block_sum(zq * zq, red);
+    const float ssk = block_sum(zk * zk, red);
+    const size_t o = ((size_t)m * H + h) * d + i;
+    q[o] = float_to_bf16_bits(ssq > 0.f ? zq / sqrtf(ssq) : 0.f);
+    k[o] = float_to_bf16_bits(ssk > 0.f ? zk / sqrtf(ssk) : 0.f);
+    v[o] = float_to_bf16_bits(zv);
+    alpha[o] = 1.0f / (1.0f + expf(zg));  // exp(-softplus(g)) = 1 / (1 + e^g)
+    if (i == 0) beta[(size_t)m * H + h] = 1.0f / (1.0f + expf(-sum(4 * Hd_ + h)));
+}
+
+__global__ void rmsnorm_kernel(int Hd, const uint16_t *__restrict__ x,
+                               const uint16_t *__restrict__ gamma, float eps, uint16_t *y) {
+    __shared__ float red[32];
+    const int m = blockIdx.x;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)m * Hd);
+    const uint4 *gr = reinterpret_cast<const uint4 *>(gamma);
+    uint4 *yr = reinterpret_cast<uint4 *>(y + (size_t)m * Hd);
+    const int nv = Hd / 8;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        const uint4 w = ld_act_v4(xr + i);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = bf16_lo(ws[j]), b = bf16_hi(ws[j]);
+            ss = __fmaf_rn(a, a, ss);
+            ss = __fmaf_rn(b, b, ss);
+        }
+    }
+    const float tot = block_sum(ss, red);
+    const float inv = 1.0f / sqrtf(tot / (float)Hd + eps);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        const uint4 w = ld_act_v4(xr + i);
+        const uint4 gg = ld_act_v4(gr + i);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w}, gs[4] = {gg.x, gg.y, gg.z, gg.w};
+        uint32_t out[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            out[j] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16_lo(ws[j]), inv), bf16_lo(gs[j])),
+                                 __fmul_rn(__fmul_rn(bf16_hi(ws[j]), inv), bf16_hi(gs[j])));
+        yr[i] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+}
+
+// One warp per token: fp32 logits (sum of split partials), top-k on logits (ties to the
+// lower index), sigmoid scores of the chosen experts, renormalised.
+__global__ void router_topk_kernel(const float *__restrict__ part, int split, int M, int E, int k,
+                                   int32_t *topk_idx, float *topk_w, float *logits_out) {
+    __shared__ float lg[1024];
+    __shared__ float sel[16];
+    const int m = blockIdx.x, lane = threadIdx.x;
+    const size_t plane = (size_t)M * E;
+    for (int e = lane; e < E; e += 32) {
+        float s = part[(size_t)m * E + e];
+        for (int sl = 1; sl < split; ++sl) s = __fadd_rn(s, part[(size_t)sl * plane + (size_t)m * E + e]);
+        lg[e] = s;
+        if (logits_out) logits_out[(size_t)m * E + e] = s;
+    }
+    __syncwarp();
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+        for (int e = lane; e < E; e += 32) {
+            const float v = lg[e];
+            if (v > bv || (v == bv && e < be)) { bv = v; be = e; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        }
+        if (lane == 0) {
+            topk_idx[(size_t)m * k + j] = be;
+            sel[j] = bv;
+            lg[be] = -INFINITY;
+        }
+        __syncwarp();
+    }
+    if (lane == 0) {
+        float sc[16], tot = 0.f;
+        for (int j = 0; j < k; ++j) {
+            sc[j] = 1.0f / (1.0f + expf(-sel[j]));
+            tot = __fadd_rn(tot, sc[j]);
+        }
+        for (int j = 0; j < k; ++j) topk_w[(size_t)m * k + j] = sc[j] / tot;
+    }
+}
+
+__global__ void l2_prefetch_kernel(const char *p, size_t bytes, uint32_t chunk) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x * chunk;
+    for (size_t off = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) * chunk; off < bytes;
+         off += stride) {
+        size_t sz = bytes - off < chunk ? bytes - off : chunk;
+        sz &= ~(size_t)15;
+        if (sz)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + off), "r"((uint32_t)sz)
+                         : "memory");
+    }
+}
+
+template <int NT>
+int launch_dense_nt(const DenseParams &p, cudaStream_t st) {
+    const long items = (long)((p.N + 15) / 16) * p.split * p.ntg;
+    const long blocks = (items * 32 + kDenseThreads - 1) / kDenseThreads;
+    trace_before(kTraceDense, st);
+    dense_stream_kernel<NT, 4><<<(unsigned)blocks, kDenseThreads, 0, st>>>(p);
+    trace_after(kTraceDense, st);
+    return launch_status();
+}
+
+}  // namespace
+
+int dense_tokens_per_tile(int M) { return M <= 8 ? 8 : 16; }
+
+// Split so that (row blocks x token groups x split) gives about 24 warp items per SM,
+// with at least 4 K steps (128 K values) per item.
+int dense_auto_split(int M, int N, int K) {
+    const char *env = getenv("HLA_DENSE_SPLIT");
+    const long nrb = (N + 15) / 16;
+    const long ntg = (M + dense_tokens_per_tile(M) - 1) / dense_tokens_per_tile(M);
+    const long base = nrb * ntg;
+    const long maxs = K / 128 > 0 ? K / 128 : 1;
+    long s = env ? atol(env) : (24L * sm_count() + base - 1) / base;
+    if (s < 1) s = 1;
+    if (s > maxs) s = maxs;
+    if (s > 64) s = 64;
+    return (int)s;
+}
+
+int router_split(int M, int Hd, int E) { return dense_auto_split(M, E, Hd); }
+
+// Run x W^T with the streaming tile.  part != nullptr -> fp32 partials [split][M][N].
+int run_dense(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W, int split, float *part,
+              void *y, int y_bf16, const hla_bf16 *residual, cudaStream_t st) {
+    DenseParams p;
+    p.W = W; p.x = x; p.M = M; p.N = N; p.K = K; p.split = split;
+    const int tt = dense_tokens_per_tile(M);
+    p.ntg = (M + tt - 1) / tt;
+    p.part = part; p.y = y; p.y_bf16 = y_bf16; p.residual = residual;
+    return tt == 8 ? launch_dense_nt<1>(p, st) : launch_dense_nt<2>(p, st);
+}
+
+int run_splitk_reduce(const float *part, int split, int M, int N, const hla_bf16 *residual, void *y,
+                      int y_bf16, cudaStream_t st) {
+    const size_t total = (size_t)M * N;
+    const int threads = 256;
+    long blocks = (long)((total + threads - 1) / threads);
+    if (blocks > 8L * sm_count()) blocks = 8L * sm_count();
+    splitk_reduce_kernel<<<(unsigned)blocks, threads, 0, st>>>(part, split, M, N, residual, y, y_bf16);
+    return launch_status();
+}
+
+int run_rmsnorm(int M, int Hd, const hla_bf16 *x, const hla_bf16 *gamma, float eps, hla_bf16 *y,
+                cudaStream_t st) {
+    rmsnorm_kernel<<<M, 256, 0, st>>>(Hd, x, gamma, eps, y);
+    return launch_status();
+}
+
+int run_l2_prefetch(const void *ptr, size_t bytes, cudaStream_t st) {
+    if (bytes < 16) return HLA_OK;
+    const uint32_t chunk = 16384;
+    long threads = (long)((bytes + chunk - 1) / chunk);
+    int blocks = (int)((threads + 127) / 128);
+    if (blocks > sm_count()) blocks = sm_count();
+    l2_prefetch_kernel<<<blocks, 128, 0, st>>>(reinterpret_cast<const char *>(ptr), bytes, chunk);
+    return launch_status();
+}
+
+int run_qkvg(int M, int Hd, int H, int d, const hla_bf16 *x, const hla_bf16 *W, hla_bf16 *q,
+             hla_bf16 *k, hla_bf16 *v, float *alpha, float *beta, int split, float *part,
+             cudaStream_t st) {
+    const int Nq = 4 * H * d + H;
+    int s = run_dense(M, Nq, Hd, x, W, split, part, nullptr, 0, nullptr, st);
+    if (s != HLA_OK) return s;
+    qkvg_epilogue_kernel<<<M * H, d, 0, st>>>(part, split, M, H, d, q, k, v, alpha, beta);
+    return launch_status();
+}
+
+int run_router(int M, int Hd, int E, int k, const hla_bf16 *x, const hla_bf16 *W_r, int32_t *idx,
+               float *w, float *logits, float *part, cudaStream_t st) {
+    const int split = router_split(M, Hd, E);
+    int s = run_dense(M, E, Hd, x, W_r, split, part, nullptr, 0, nullptr, st);
+    if (s != HLA_OK) return s;
+    router_topk_kernel<<<M, 32, 0, st>>>(part, split, M, E, k, idx, w, logits);
+    return launch_status();
+}
+
+}  // namespace hla
+
+using namespace hla;
+
+static int resolve_split(int M, int N, int K, int split) {
+    return split > 0 ? (split > K / 32 ? K / 32 : split) : dense_auto_split(M, N, K);
+}
+
+extern "C" size_t skinny_proj_splitk_workspace_size(int M, int N, int K, int split) {
+    if (M < 1 || N < 1 || K < 32) return 0;
+    const int s = resolve_split(M, N, K, split);
+    return s > 1 ? (size_t)s * M * N * sizeof(float) : 0;
+}
+
+extern "C" int skinny_proj_splitk(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W,
+                                  const hla_bf16 *residual, void *y, int y_dtype, int split,
+                                  void *ws, size_t ws_bytes, hla_stream stream) {
+    HLA_REQUIRE(M >= 1 && N >= 1 && K >= 32 && split >= 0, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(M <= 256 && K % 32 == 0, HLA_ERR_UNSUPPORTED);
+    HLA_REQUIRE(x && W && y, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(y_dtype == HLA_F32 || y_dtype == HLA_BF16, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(aligned16(x) && aligned16(W) && aligned16(y) && (!residual || aligned16(residual)),
+                HLA_ERR_MISALIGNED);
+    const int s = resolve_split(M, N, K, split);
+    const size_t need = skinny_proj_splitk_workspace_size(M, N, K, split);
+    HLA_REQUIRE(need == 0 || (ws && ws_bytes >= need), HLA_ERR_WORKSPACE);
+    HLA_REQUIRE(need == 0 || aligned16(ws), HLA_ERR_MISALIGNED);
+    cudaStream_t st = (cudaStream_t)stream;
+    set_variant("skinny_proj<tt%d,split%d>", dense_tokens_per_tile(M), s);
+    if (s == 1) return run_dense(M, N, K, x, W, 1, nullptr, y, y_dtype == HLA_BF16, residual, st);
+    int r = run_dense(M, N, K, x, W, s, reinterpret_cast<float *>(ws), nullptr, 0, nullptr, st);
+    if (r != HLA_OK) return r;
+    return run_splitk_reduce(reinterpret_cast<float *>(ws), s, M, N, residual, y, y_dtype == HLA_BF16, st);
+}
+
+extern "C" size_t kda_qkvg_proj_workspace_size(int M, int Hd, int H, int dk, int dv, int split) {
+    if (M < 1 || Hd < 32 || H < 1 || dk < 1 || dv != dk) return 0;
+    const int Nq = 4 * H * dk + H;
+    const int s = resolve_split(M, Nq, Hd, split);
+    return (size_t)s * M * Nq * sizeof(float);
+}
+
+extern "C" int kda_qkvg_proj(int M, int Hd, int H, int dk, int dv, const hla_bf16 *x,
+                             const hla_bf16 *W, hla_bf16 *q, hla_bf16 *k, hla_bf16 *v, float *alpha,
+                             float *beta, int split, void *ws, size_t ws_bytes, hla_stream stream) {
+    HLA_REQUIRE(M >= 1 && Hd >= 32 && H >= 1 && split >= 0, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(dk == dv && (dk == 64 || dk == 128) && M <= 256 && Hd % 32 == 0, HLA_ERR_UNSUPPORTED);
+    HLA_REQUIRE(x && W && q && k && v && alpha && beta, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(aligned16(x) && aligned16(W) && aligned16(q) && aligned16(k) && aligned16(v) &&
+                    aligned16(alpha) && aligned16(beta),
+                HLA_ERR_MISALIGNED);
+    const size_t need = kda_qkvg_proj_workspace_size(M, Hd, H, dk, dv, split);
+    HLA_REQUIRE(ws && ws_bytes >= need, HLA_ERR_WORKSPACE);
+    HLA_REQUIRE(aligned16(ws), HLA_ERR_MISALIGNED);
+    const int s = resolve_split(M, 4 * H * dk + H, Hd, split);
+    set_variant("qkvg_proj<tt%d,split%d>", dense_tokens_per_tile(M), s);
+    return run_qkvg(M, Hd, H, dk, x, W, q, k, v, alpha, beta, s, reinterpret_cast<float *>(ws),
+                    (cudaStream_t)stream);
+}
+
+extern "C" int hla_rmsnorm(int M, int Hd, const hla_bf16 *x, const hla_bf16 *gamma, float eps,
+                           hla_bf16 *y, hla_stream stream) {
+    HLA_REQUIRE(M >= 1 && Hd >= 8 && eps >= 0.f, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(Hd % 8 == 0 && M <= 65535, HLA_ERR_UNSUPPORTED);
+    HLA_REQUIRE(x && gamma && y, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(aligned16(x) && aligned16(gamma) && aligned16(y), HLA_ERR_MISALIGNED);
+    set_variant("rmsnorm");
+    return run_rmsnorm(M, Hd, x, gamma, eps, y, (cudaStream_t)stream);
+}
+
+extern "C" size_t moe_route_topk_workspace_size(int M, int Hd, int E) {
+    if (M < 1 || Hd < 32 || E < 1) return 0;
+    return (size_t)router_split(M, Hd, E) * M * E * sizeof(float);
+}
+
+extern "C" int moe_route_topk(int M, int Hd, int E, int k, const hla_bf16 *x, const hla_bf16 *W_r,
+                              int32_t *topk_idx, float *topk_w, float *logits, void *ws,
+                              size_t ws_bytes, hla_stream stream) {
+    HLA_REQUIRE(M >= 1 && Hd >= 32 && E >= 1 && k >= 1, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(k <= 16 && k <= E && E <= 1024 && Hd % 32 == 0 && M <= 65535, HLA_ERR_UNSUPPORTED);
+    HLA_REQUIRE(x && W_r && topk_idx && topk_w, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(aligned16(x) && aligned16(W_r) && aligned16(topk_idx) && aligned16(topk_w) &&
+                    (!logits || aligned16(logits)),
+                HLA_ERR_MISALIGNED);
+    const size_t need = moe_route_topk_workspace_size(M, Hd, E);
+    HLA_REQUIRE(ws && ws_bytes >= need, HLA_ERR_WORKSPACE);
+    HLA_REQUIRE(aligned16(ws), HLA_ERR_MISALIGNED);
+    set_variant("router<split%d>", router_split(M, Hd, E));
+    return run_router(M, Hd, E, k, x, W_r, topk_idx, topk_w, logits, reinterpret_cast<float *>(ws),
+                      (cudaStream_t)stream);
+}
+
+extern "C" int hla_l2_prefetch(const void *ptr, size_t bytes, hla_stream stream) {
+    HLA_REQUIRE(ptr || bytes == 0, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(bytes == 0 || aligned16(ptr), HLA_ERR_MISALIGNED);
+    set_variant("l2_prefetch");
+    return run_l2_prefetch(ptr, bytes, (cudaStream_t)stream);
+}

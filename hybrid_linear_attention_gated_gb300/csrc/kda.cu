@@ -1,0 +1,292 @@
+// KDA recurrent-state kernels: decode step, speculative verify, accepted-prefix replay,
+// and the accepted-length bookkeeping.
+//
+// The update is the gated delta rule (KDA's fixed-size recurrent state, "Kimi K3:
+// From Day-0 Availability to Optimized Inference"):
+//     S' = diag(alpha) S                (rows scaled by the per-key decay)
+//     u  = S'^T k,  w = S'^T q          (one pass over S' gives both)
+//     S_t = S' + beta k (v - u)^T        (= (I - beta k k^T) S' + beta k v^T)
+//     o   = w + beta (q.k) (v - u)       (= S_t^T q, read from the updated state)
+// Column j of S_t depends only on column j of S, so a (sequence, head) state
+// splits over d_v into independent column slices; small batches use narrow
+// slices to put work on every SM ("KDA decode kernel ... scheduling tuned for the
+// batch size and number of heads", "Hyper-optimizing Kimi K3 in vLLM", Part 1 sec. 1).
+//
+// Layout inside a CTA: 8 row groups x (CW/4) float4 column groups.  Thread
+// (rg, cg) keeps rows rg, rg+8, rg+16, ... of 4 columns in registers, so the state
+// is read from HBM once and written once.  The row partition (and therefore the
+// order of every reduction) is the same for every slice width, which makes the
+// result independent of the variant chosen: replaying T tokens is bit-identical to
+// T single decode steps.
+#include <cstdlib>
+
+#include "common.cuh"
+
+namespace hla {
+namespace {
+
+constexpr int kRowGroups = 8;
+constexpr int kMaxWindow = 8;
+
+enum KdaMode { kDecode = 0, kVerify = 1, kReplay = 2 };
+
+struct KdaParams {
+    float *S;
+    const int32_t *state_idx;
+    const uint16_t *q, *k, *v;
+    const float *alpha, *beta;
+    const int32_t *accepted;
+    void *o;
+    int o_bf16;
+    int B, T, H;
+};
+
+template <int DK, int CW, int MODE>
+__global__ void __launch_bounds__(kRowGroups *CW / 4)
+    kda_recur_kernel(const KdaParams p) {
+    constexpr int CG = CW / 4;
+    constexpr int RPT = DK / kRowGroups;
+    constexpr int DV = DK;
+    constexpr int NSLICE = DV / CW;
+    constexpr int NTHR = kRowGroups * CG;
+    constexpr int TMAX = MODE == kDecode ? 1 : kMaxWindow;
+
+    __shared__ float sq[TMAX][DK], sk[TMAX][DK], sa[TMAX][DK], sv[TMAX][CW], sb[TMAX];
+    __shared__ float4 red_u[2][kRowGroups][CG], red_w[2][kRowGroups][CG];
+    __shared__ float red_qk[2][kRowGroups];
+
+    const int tid = threadIdx.x;
+    const int cg = tid % CG;
+    const int rg = tid / CG;
+    const int slice = blockIdx.x % NSLICE;
+    const int bh = blockIdx.x / NSLICE;
+    const int h = bh % p.H;
+    const int b = bh / p.H;
+    const int col0 = slice * CW;
+
+    int steps = MODE == kDecode ? 1 : p.T;
+    if (MODE == kReplay) {
+        const int a = p.accepted[b];
+        steps = a < 0 ? 0 : (a > p.T ? p.T : a);
+        if (steps == 0) return;  // nothing accepted: the committed state is not touched
+    }
+
+    const int slot = p.state_idx ? p.state_idx[b] : b;
+    float *Sb = p.S + ((size_t)slot * p.H + h) * (size_t)(DK * DV) + col0 + cg * 4;
+
+    float4 s[RPT];
+#pragma unroll
+    for (int j = 0; j < RPT; ++j)
+        s[j] = *reinterpret_cast<const float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV);
+
+    // the window's per-token vectors (token t of sequence b is row (b*T + t) of [B, T, H, .])
+    const int Tld = MODE == kDecode ? 1 : p.T;
+    for (int t = 0; t < steps; ++t) {
+        const size_t tok = ((size_t)b * Tld + t) * p.H + h;
+        for (int i = tid; i < DK; i += NTHR) {
+            sq[t][i] = bf16_bits_to_float(p.q[tok * DK + i]);
+            sk[t][i] = bf16_bits_to_float(p.k[tok * DK + i]);
+            sa[t][i] = p.alpha[tok * DK + i];
+        }
+        for (int c = tid; c < CW; c += NTHR) sv[t][c] = bf16_bits_to_float(p.v[tok * DV + col0 + c]);
+        if (tid == 0) sb[t] = p.beta[tok];
+    }
+    __syncthreads();
+
+    for (int t = 0; t < steps; ++t) {
+        const int buf = t & 1;
+        float4 pu = make_float4(0.f, 0.f, 0.f, 0.f), pw = pu;
+        float pqk = 0.f;
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+            const int i = rg + kRowGroups * j;
+            const float a = sa[t][i], kk = sk[t][i], qq = sq[t][i];
+            s[j].x = __fmul_rn(s[j].x, a);
+            s[j].y = __fmul_rn(s[j].y, a);
+            s[j].z = __fmul_rn(s[j].z, a);
+            s[j].w = __fmul_rn(s[j].w, a);
+            pu.x = __fmaf_rn(kk, s[j].x, pu.x);
+            pu.y = __fmaf_rn(kk, s[j].y, pu.y);
+            pu.z = __fmaf_rn(kk, s[j].z, pu.z);
+            pu.w = __fmaf_rn(kk, s[j].w, pu.w);
+            pw.x = __fmaf_rn(qq, s[j].x, pw.x);
+            pw.y = __fmaf_rn(qq, s[j].y, pw.y);
+            pw.z = __fmaf_rn(qq, s[j].z, pw.z);
+            pw.w = __fmaf_rn(qq, s[j].w, pw.w);
+            pqk = __fmaf_rn(qq, kk, pqk);
+        }
+        red_u[buf][rg][cg] = pu;
+        red_w[buf][rg][cg] = pw;
+        if (cg == 0) red_qk[buf][rg] = pqk;
+        __syncthreads();
+
+        float4 u = red_u[buf][0][cg], w = red_w[buf][0][cg];
+        float qk = red_qk[buf][0];
+#pragma unroll
+        for (int r = 1; r < kRowGroups; ++r) {
+            const float4 ur = red_u[buf][r][cg], wr = red_w[buf][r][cg];
+            u.x = __fadd_rn(u.x, ur.x); u.y = __fadd_rn(u.y, ur.y);
+            u.z = __fadd_rn(u.z, ur.z); u.w = __fadd_rn(u.w, ur.w);
+            w.x = __fadd_rn(w.x, wr.x); w.y = __fadd_rn(w.y, wr.y);
+            w.z = __fadd_rn(w.z, wr.z); w.w = __fadd_rn(w.w, wr.w);
+            qk = __fadd_rn(qk, red_qk[buf][r]);
+        }
+        const float bt = sb[t];
+        float4 d;
+        d.x = __fmul_rn(bt, __fsub_rn(sv[t][cg * 4 + 0], u.x));
+        d.y = __fmul_rn(bt, __fsub_rn(sv[t][cg * 4 + 1], u.y));
+        d.z = __fmul_rn(bt, __fsub_rn(sv[t][cg * 4 + 2], u.z));
+        d.w = __fmul_rn(bt, __fsub_rn(sv[t][cg * 4 + 3], u.w));
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+            const float kk = sk[t][rg + kRowGroups * j];
+            s[j].x = __fmaf_rn(kk, d.x, s[j].x);
+            s[j].y = __fmaf_rn(kk, d.y, s[j].y);
+            s[j].z = __fmaf_rn(kk, d.z, s[j].z);
+            s[j].w = __fmaf_rn(kk, d.w, s[j].w);
+        }
+        if (MODE != kReplay && rg == 0) {
+            float4 o;
+            o.x = __fmaf_rn(qk, d.x, w.x);
+            o.y = __fmaf_rn(qk, d.y, w.y);
+            o.z = __fmaf_rn(qk, d.z, w.z);
+            o.w = __fmaf_rn(qk, d.w, w.w);
+            const size_t oo = (((size_t)b * Tld + t) * p.H + h) * DV + col0 + cg * 4;
+            if (p.o_bf16) {
+                uint2 pk = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+                *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.o) + oo) = pk;
+            } else {
+                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + oo) = o;
+            }
+        }
+    }
+
+    if (MODE != kVerify) {
+#pragma unroll
+        for (int j = 0; j < RPT; ++j)
+            *reinterpret_cast<float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV) = s[j];
+    }
+}
+
+template <int DK, int MODE>
+int launch_dk(int cw, const KdaParams &p, cudaStream_t st) {
+    const int grid_per_head = DK / cw;
+    const dim3 grid((unsigned)((size_t)p.B * p.H * grid_per_head));
+    trace_before(kTraceKda, st);
+    switch (cw) {
+        case 16: kda_recur_kernel<DK, 16, MODE><<<grid, kRowGroups * 4, 0, st>>>(p); break;
+        case 32: kda_recur_kernel<DK, 32, MODE><<<grid, kRowGroups * 8, 0, st>>>(p); break;
+        case 64: kda_recur_kernel<DK, 64, MODE><<<grid, kRowGroups * 16, 0, st>>>(p); break;
+        case 128:
+            if constexpr (DK >= 128) {
+                kda_recur_kernel<DK, 128, MODE><<<grid, kRowGroups * 32, 0, st>>>(p);
+                break;
+            } else {
+                return HLA_ERR_UNSUPPORTED;
+            }
+        default: return HLA_ERR_UNSUPPORTED;
+    }
+    trace_after(kTraceKda, st);
+    return launch_status();
+}
+
+// Column-slice width: the widest slice that still gives about two CTAs per SM.
+int choose_cw(int B, int H, int dv) {
+    const char *env = getenv("HLA_KDA_CW");
+    if (env) {
+        const int v = atoi(env);
+        if ((v == 16 || v == 32 || v == 64 || v == 128) && v <= dv) return v;
+    }
+    const long heads = (long)B * H;
+    const long target = 2L * sm_count();
+    int cw = dv;
+    while (cw > 16 && heads * (dv / cw) < target) cw /= 2;
+    return cw;
+}
+
+int run_kda(int mode, int B, int T, int H, int dk, int dv, float *S, const int32_t *state_idx,
+            const hla_bf16 *q, const hla_bf16 *k, const hla_bf16 *v, const float *alpha,
+            const float *beta, const int32_t *accepted, void *o, int o_dtype, cudaStream_t st) {
+    HLA_REQUIRE(B >= 1 && H >= 1 && T >= 1, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(dk == dv && (dk == 64 || dk == 128), HLA_ERR_UNSUPPORTED);
+    HLA_REQUIRE(T <= kMaxWindow, HLA_ERR_UNSUPPORTED);
+    HLA_REQUIRE((long)B * H * (dv / 16) < (1L << 31), HLA_ERR_UNSUPPORTED);
+    HLA_REQUIRE(S && q && k && v && alpha && beta, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(mode != kReplay || accepted, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(mode == kReplay || o, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(o_dtype == HLA_F32 || o_dtype == HLA_BF16, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(aligned16(S) && aligned16(q) && aligned16(k) && aligned16(v) && aligned16(alpha) &&
+                    aligned16(beta) && (o == nullptr || aligned16(o)) &&
+                    (state_idx == nullptr || aligned16(state_idx)) &&
+                    (accepted == nullptr || aligned16(accepted)),
+                HLA_ERR_MISALIGNED);
+    KdaParams p;
+    p.S = S; p.state_idx = state_idx; p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
+    p.accepted = accepted; p.o = o; p.o_bf16 = o_dtype == HLA_BF16; p.B = B; p.T = T; p.H = H;
+    const int cw = choose_cw(B, H, dv);
+    static const char *names[3] = {"decode", "verify", "replay"};
+    set_variant("kda_recur<dk%d,cw%d,%s>", dk, cw, names[mode]);
+    int st_ = HLA_ERR_UNSUPPORTED;
+    if (dk == 128) {
+        st_ = mode == kDecode ? launch_dk<128, kDecode>(cw, p, st)
+            : mode == kVerify ? launch_dk<128, kVerify>(cw, p, st)
+                              : launch_dk<128, kReplay>(cw, p, st);
+    } else {
+        st_ = mode == kDecode ? launch_dk<64, kDecode>(cw, p, st)
+            : mode == kVerify ? launch_dk<64, kVerify>(cw, p, st)
+                              : launch_dk<64, kReplay>(cw, p, st);
+    }
+    return st_;
+}
+
+__global__ void accept_prefix_kernel(int B, int T, const int32_t *__restrict__ draft,
+                                     const int32_t *__restrict__ target, int32_t *accepted,
+                                     int32_t *committed) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    int n = 0;
+    while (n < T && draft[(size_t)b * T + n] == target[(size_t)b * T + n]) ++n;
+    accepted[b] = n;
+    committed[b] += n;
+}
+
+}  // namespace
+}  // namespace hla
+
+using namespace hla;
+
+extern "C" int kda_decode_step(int B, int H, int dk, int dv, float *S, const int32_t *state_idx,
+                               const hla_bf16 *q, const hla_bf16 *k, const hla_bf16 *v,
+                               const float *alpha, const float *beta, void *o, int o_dtype,
+                               hla_stream stream) {
+    return run_kda(kDecode, B, 1, H, dk, dv, S, state_idx, q, k, v, alpha, beta, nullptr, o,
+                   o_dtype, (cudaStream_t)stream);
+}
+
+extern "C" int kda_spec_verify_replay(int phase, int B, int T, int H, int dk, int dv, float *S,
+                                      const int32_t *state_idx, const hla_bf16 *q,
+                                      const hla_bf16 *k, const hla_bf16 *v, const float *alpha,
+                                      const float *beta, const int32_t *accepted_len, void *o,
+                                      int o_dtype, hla_stream stream) {
+    if (phase == HLA_SPEC_VERIFY)
+        return run_kda(kVerify, B, T, H, dk, dv, S, state_idx, q, k, v, alpha, beta, nullptr, o,
+                       o_dtype, (cudaStream_t)stream);
+    if (phase == HLA_SPEC_REPLAY)
+        return run_kda(kReplay, B, T, H, dk, dv, S, state_idx, q, k, v, alpha, beta,
+                       accepted_len, nullptr, o_dtype, (cudaStream_t)stream);
+    return HLA_ERR_INVALID_ARG;
+}
+
+extern "C" int spec_accept_prefix(int B, int T, const int32_t *draft_ids,
+                                  const int32_t *target_ids, int32_t *accepted_len,
+                                  int32_t *committed_len, hla_stream stream) {
+    HLA_REQUIRE(B >= 1 && T >= 1 && T <= 64, B >= 1 && T >= 1 ? HLA_ERR_UNSUPPORTED : HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(draft_ids && target_ids && accepted_len && committed_len, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(aligned16(draft_ids) && aligned16(target_ids) && aligned16(accepted_len) &&
+                    aligned16(committed_len),
+                HLA_ERR_MISALIGNED);
+    set_variant("accept_prefix");
+    accept_prefix_kernel<<<(B + 127) / 128, 128, 0, (cudaStream_t)stream>>>(
+        B, T, draft_ids, target_ids, accepted_len, committed_len);
+    return launch_status();
+}

@@ -1,0 +1,512 @@
+// Routed + shared SwiGLU experts at decode batch sizes.
+//
+// "Kimi K3: From Day-0 Availability to Optimized Inference": at low batch, moving
+// expert weights through GPU memory is the limit.  "Hyper-optimizing Kimi K3 in
+// vLLM", Part 1 sec. 3: routed experts plus a shared expert for every token;
+// sec. 4: a side-stream kernel warms L2 with upcoming weights while a phase cannot
+// use the memory bandwidth.
+//
+// Pipeline (all on device, no host round trip; sizes the host does not know -- the
+// number of active experts -- are read by persistent kernels from the workspace):
+//   1. dispatch   : one CTA groups the M*k (token, slot) pairs by expert (counting
+//                   sort, stable by pair index), lists the active experts (shared
+//                   experts first) and prefix-sums their work items.
+//   2. gate/up    : persistent warps stream 16 rows of W_gate[e] and W_up[e] over a
+//                   K slice for up to 16 of expert e's tokens; SiLU(g)*u -> h (bf16),
+//                   or fp32 partials when K is split (small M, to fill the GPU).
+//   3. [reduce]   : h = SiLU(sum g) * (sum u) over the K slices, fixed order.
+//   4. down       : persistent warps stream 16 rows of W_down[e] for the tokens'
+//                   h rows -> one fp32 row per (token, slot).
+//   5. combine    : y[m] = sum_j w[m,j] * y[m,j] + sum_s y[m,k+s] (+ residual), fixed order.
+// Each active expert's weights are read from HBM once per call; when an expert has
+// more than 16 tokens, its token groups are adjacent work items that stream the same
+// rows at the same time, so the repeats are served by L2.
+#include <cstdlib>
+
+#include "common.cuh"
+#include "stream_mma.cuh"
+
+namespace hla {
+
+int run_l2_prefetch(const void *ptr, size_t bytes, cudaStream_t st);
+
+namespace {
+
+constexpr int kMoeThreads = 128;
+constexpr int kDispatchThreads = 1024;
+
+struct MoeLayout {
+    int M, Hd, I, E, k, nsh, P, U_max, KS, TT;
+    size_t off_meta, off_unit_expert, off_unit_off, off_item_gu, off_item_dn, off_pos_token,
+        off_pos_slot, off_h, off_part_g, off_part_u, off_ypart, total;
+};
+
+struct MoeArgs {
+    int M, Hd, I, E, k, nsh, P, KS, TT;
+    const uint16_t *x;
+    const int32_t *topk_idx;
+    const float *topk_w;
+    const uint16_t *W_gate, *W_up, *W_down, *Ws_gate, *Ws_up, *Ws_down;
+    const uint16_t *residual;
+    uint16_t *y;
+    int *meta, *unit_expert, *unit_off, *item_gu, *item_dn, *pos_token, *pos_slot;
+    uint16_t *h;
+    float *part_g, *part_u, *ypart;
+};
+
+int moe_tokens_per_tile(int M) { return M <= 8 ? 8 : 16; }
+
+int moe_gateup_split(int M, int I, int E, int k, int nsh) {
+    const char *env = getenv("HLA_MOE_SPLIT");
+    if (env) {
+        const int v = atoi(env);
+        if (v >= 1 && v <= 16) return v;
+    }
+    long units = (long)M * k < E ? (long)M * k : E;
+    units += nsh;
+    const long items = units * ((I + 15) / 16);
+    long s = (24L * sm_count() + items - 1) / items;
+    if (s < 1) s = 1;
+    if (s > 8) s = 8;
+    return (int)s;
+}
+
+MoeLayout moe_layout(int M, int Hd, int I, int E, int k, int nsh) {
+    MoeLayout L;
+    L.M = M; L.Hd = Hd; L.I = I; L.E = E; L.k = k; L.nsh = nsh;
+    L.P = M * (k + nsh);
+    L.U_max = E + nsh;
+    L.KS = moe_gateup_split(M, I, E, k, nsh);
+    L.TT = moe_tokens_per_tile(M);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = round_up(o + bytes, 256);
+        return at;
+    };
+    L.off_meta = take(16 * sizeof(int));
+    L.off_unit_expert = take((size_t)L.U_max * sizeof(int));
+    L.off_unit_off = take((size_t)(L.U_max + 1) * sizeof(int));
+    L.off_item_gu = take((size_t)(L.U_max + 1) * sizeof(int));
+    L.off_item_dn = take((size_t)(L.U_max + 1) * sizeof(int));
+    L.off_pos_token = take((size_t)L.P * sizeof(int));
+    L.off_pos_slot = take((size_t)L.P * sizeof(int));
+    L.off_h = take((size_t)L.P * I * sizeof(uint16_t));
+    L.off_part_g = take(L.KS > 1 ? (size_t)L.KS * L.P * I * sizeof(float) : 0);
+    L.off_part_u = take(L.KS > 1 ? (size_t)L.KS * L.P * I * sizeof(float) : 0);
+    L.off_ypart = take((size_t)L.P * Hd * sizeof(float));
+    L.total = o;
+    return L;
+}
+
+// Exclusive prefix sum over one value per thread of a kDispatchThreads-thread block.
+__device__ int block_exclusive_scan(int v, int *warp_tot, int &total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    __syncthreads();
+    if (lane == 31) warp_tot[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        const int t = warp_tot[lane];
+        int s = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += n;
+        }
+        warp_tot[lane] = s - t;  // exclusive warp offsets
+        if (lane == 31) warp_tot[32] = s;
+    }
+    __syncthreads();
+    total = warp_tot[32];
+    return warp_tot[w] + incl - v;
+}
+
+__global__ void __launch_bounds__(kDispatchThreads) moe_dispatch_kernel(const MoeArgs a) {
+    __shared__ int cnt[1024], base[1024], run[1024], uid[1024];
+    __shared__ int warp_tot[33];
+    const int tid = threadIdx.x;
+    const int npairs = a.M * a.k;
+    const int nrb_gu = (a.I + 15) / 16, nrb_dn = (a.Hd + 15) / 16;
+
+    cnt[tid] = 0;
+    run[tid] = 0;
+    __syncthreads();
+    for (int p = tid; p < npairs; p += kDispatchThreads) {
+        const int e = a.topk_idx[p];
+        if (e >= 0 && e < a.E) atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    const int c = tid < a.E ? cnt[tid] : 0;
+    int nvalid, nact;
+    base[tid] = block_exclusive_scan(c, warp_tot, nvalid);
+    uid[tid] = block_exclusive_scan(c > 0 ? 1 : 0, warp_tot, nact);
+    __syncthreads();
+
+    const int routed0 = a.nsh * a.M;  // shared experts' positions come first
+    if (tid < 32) {
+        // stable placement: pairs in increasing index order within each expert
+        const unsigned lt = (1u << tid) - 1u;
+        for (int c0 = 0; c0 < npairs; c0 += 32) {
+            const int p = c0 + tid;
+            const int e = p < npairs ? a.topk_idx[p] : -1;
+            const bool valid = e >= 0 && e < a.E;
+            const unsigned grp = __match_any_sync(0xffffffffu, valid ? e : -1 - tid);
+            if (valid) {
+                const int pos = routed0 + base[e] + run[e] + __popc(grp & lt);
+                const int m = p / a.k, j = p % a.k;
+                a.pos_token[pos] = m;
+                a.pos_slot[pos] = m * (a.k + a.nsh) + j;
+            }
+            __syncwarp();
+            if (valid && (grp & lt) == 0) run[e] += __popc(grp);
+            __syncwarp();
+        }
+    }
+    for (int i = tid; i < routed0; i += kDispatchThreads) {
+        const int s = i / a.M, m = i % a.M;
+        a.pos_token[i] = m;
+        a.pos_slot[i] = m * (a.k + a.nsh) + a.k + s;
+    }
+    // unit tables: shared experts are units 0..nsh-1, routed experts follow by id
+    if (tid < a.nsh) {
+        a.unit_expert[tid] = a.E + tid;
+        a.unit_off[tid] = tid * a.M;
+    }
+    if (tid < a.E && c > 0) {
+        a.unit_expert[a.nsh + uid[tid]] = tid;
+        a.unit_off[a.nsh + uid[tid]] = routed0 + base[tid];
+    }
+    const int U = a.nsh + nact;
+    if (tid == 0) {
+        a.unit_off[U] = routed0 + nvalid;
+        a.meta[0] = U;
+    }
+    __syncthreads();
+    int ig = 0, id = 0;
+    if (tid < U) {
+        const int n = a.unit_off[tid + 1] - a.unit_off[tid];
+        const int ntg = (n + a.TT - 1) / a.TT;
+        ig = nrb_gu * a.KS * ntg;
+        id = nrb_dn * ntg;
+    }
+    int tot_g, tot_d;
+    const int og = block_exclusive_scan(ig, warp_tot, tot_g);
+    const int od = block_exclusive_scan(id, warp_tot, tot_d);
+    if (tid < U) {
+        a.item_gu[tid] = og;
+        a.item_dn[tid] = od;
+    }
+    if (tid == 0) {
+        a.item_gu[U] = tot_g;
+        a.item_dn[U] = tot_d;
+        a.meta[1] = tot_g;
+        a.meta[2] = tot_d;
+    }
+}
+
+// largest u in [0, U) with pref[u] <= it
+__device__ __forceinline__ int find_unit(const int *pref, int U, int it) {
+    int lo = 0, hi = U - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pref[mid] <= it) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kMoeThreads) moe_gateup_kernel(const MoeArgs a) {
+    const int U = a.meta[0];
+    const int total = a.item_gu[U];
+    const int nwarps = gridDim.x * (kMoeThreads / 32);
+    const int g = (threadIdx.x & 31) >> 2;
+    const int nrb = (a.I + 15) / 16;
+    for (int it = blockIdx.x * (kMoeThreads / 32) + (threadIdx.x >> 5); it < total; it += nwarps) {
+        const int u = find_unit(a.item_gu, U, it);
+        const int local = it - a.item_gu[u];
+        const int p0 = a.unit_off[u], p1 = a.unit_off[u + 1];
+        const int ntg = (p1 - p0 + a.TT - 1) / a.TT;
+        const int tg = local % ntg;
+        const int rest = local / ntg;
+        const int ks = rest % a.KS;
+        const int rb = rest / a.KS;
+        (void)nrb;
+        const int e = a.unit_expert[u];
+        const size_t eoff = (size_t)(e < a.E ? e : e - a.E) * a.I * a.Hd;
+        const uint16_t *Wg = (e < a.E ? a.W_gate : a.Ws_gate) + eoff;
+        const uint16_t *Wu = (e < a.E ? a.W_up : a.Ws_up) + eoff;
+        const int r0 = min(rb * 16 + g, a.I - 1), r1 = min(rb * 16 + g + 8, a.I - 1);
+        const uint16_t *wg[2] = {Wg + (size_t)r0 * a.Hd, Wu + (size_t)r0 * a.Hd};
+        const uint16_t *wg8[2] = {Wg + (size_t)r1 * a.Hd, Wu + (size_t)r1 * a.Hd};
+        const int pt = p0 + tg * a.TT;
+        const uint16_t *xr[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int p = pt + nt * 8 + g;
+            xr[nt] = a.x + (size_t)a.pos_token[p < p1 ? p : pt] * a.Hd;
+        }
+        int kb, ke;
+        k_slice(a.Hd, a.KS, ks, kb, ke);
+        float acc[2][NT][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[m][nt][q] = 0.f;
+        warp_stream_tile<2, NT, 4>(wg, wg8, xr, kb, ke, acc);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int row = rb * 16 + acc_row(q);
+                const int p = pt + acc_tok(nt, q);
+                if (row >= a.I || p >= p1) continue;
+                if (a.KS == 1) {
+                    a.h[(size_t)p * a.I + row] =
+                        float_to_bf16_bits(__fmul_rn(silu_f(acc[0][nt][q]), acc[1][nt][q]));
+                } else {
+                    const size_t o = ((size_t)ks * a.P + p) * a.I + row;
+                    a.part_g[o] = acc[0][nt][q];
+                    a.part_u[o] = acc[1][nt][q];
+                }
+            }
+        }
+    }
+}
+
+__global__ void moe_swiglu_reduce_kernel(const MoeArgs a) {
+    const int n = a.meta[0];
+    const int used = a.unit_off[n];  // positions in use
+    const size_t total = (size_t)used * a.I, plane = (size_t)a.P * a.I;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        float g = a.part_g[i], u = a.part_u[i];
+        for (int s = 1; s < a.KS; ++s) {
+            g = __fadd_rn(g, a.part_g[s * plane + i]);
+            u = __fadd_rn(u, a.part_u[s * plane + i]);
+        }
+        a.h[i] = float_to_bf16_bits(__fmul_rn(silu_f(g), u));
+    }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(const MoeArgs a) {
+    const int U = a.meta[0];
+    const int total = a.item_dn[U];
+    const int nwarps = gridDim.x * (kMoeThreads / 32);
+    const int g = (threadIdx.x & 31) >> 2;
+    for (int it = blockIdx.x * (kMoeThreads / 32) + (threadIdx.x >> 5); it < total; it += nwarps) {
+        const int u = find_unit(a.item_dn, U, it);
+        const int local = it - a.item_dn[u];
+        const int p0 = a.unit_off[u], p1 = a.unit_off[u + 1];
+        const int ntg = (p1 - p0 + a.TT - 1) / a.TT;
+        const int tg = local % ntg;
+        const int rb = local / ntg;
+        const int e = a.unit_expert[u];
+        const uint16_t *Wd = (e < a.E ? a.W_down : a.Ws_down) +
+                             (size_t)(e < a.E ? e : e - a.E) * a.Hd * a.I;
+        const int r0 = min(rb * 16 + g, a.Hd - 1), r1 = min(rb * 16 + g + 8, a.Hd - 1);
+        const uint16_t *wg[1] = {Wd + (size_t)r0 * a.I};
+        const uint16_t *wg8[1] = {Wd + (size_t)r1 * a.I};
+        const int pt = p0 + tg * a.TT;
+        const uint16_t *xr[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int p = pt + nt * 8 + g;
+            xr[nt] = a.h + (size_t)(p < p1 ? p : pt) * a.I;
+        }
+        float acc[1][NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[0][nt][q] = 0.f;
+        warp_stream_tile<1, NT, 4>(wg, wg8, xr, 0, a.I, acc);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int row = rb * 16 + acc_row(q);
+                const int p = pt + acc_tok(nt, q);
+                if (row >= a.Hd || p >= p1) continue;
+                a.ypart[(size_t)a.pos_slot[p] * a.Hd + row] = acc[0][nt][q];
+            }
+        }
+    }
+}
+
+__global__ void moe_combine_kernel(const MoeArgs a) {
+    const int m = blockIdx.y;
+    const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c4 * 4 >= a.Hd) return;
+    const int S = a.k + a.nsh;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < S; ++j) {
+        float w = 1.0f;
+        if (j < a.k) {
+            const int e = a.topk_idx[(size_t)m * a.k + j];
+            if (e < 0 || e >= a.E) continue;
+            w = a.topk_w[(size_t)m * a.k + j];
+        }
+        const float4 v = reinterpret_cast<const float4 *>(a.ypart + ((size_t)m * S + j) * a.Hd)[c4];
+        acc.x = __fmaf_rn(w, v.x, acc.x);
+        acc.y = __fmaf_rn(w, v.y, acc.y);
+        acc.z = __fmaf_rn(w, v.z, acc.z);
+        acc.w = __fmaf_rn(w, v.w, acc.w);
+    }
+    const size_t o = (size_t)m * a.Hd + (size_t)c4 * 4;
+    if (a.residual) {
+        const uint2 r = *reinterpret_cast<const uint2 *>(a.residual + o);
+        acc.x = __fadd_rn(acc.x, bf16_lo(r.x));
+        acc.y = __fadd_rn(acc.y, bf16_hi(r.x));
+        acc.z = __fadd_rn(acc.z, bf16_lo(r.y));
+        acc.w = __fadd_rn(acc.w, bf16_hi(r.y));
+    }
+    *reinterpret_cast<uint2 *>(a.y + o) =
+        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+}
+
+template <typename K>
+int persistent_grid(K kernel) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kMoeThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    return per_sm * sm_count();
+}
+
+struct SideStreamEvents {
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool ok() {
+        if (!fork && cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess) return false;
+        if (!join && cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) return false;
+        return true;
+    }
+};
+thread_local SideStreamEvents g_moe_events;
+
+}  // namespace
+
+size_t moe_workspace_bytes(int M, int Hd, int I, int E, int k, int nsh) {
+    return moe_layout(M, Hd, I, E, k, nsh).total;
+}
+
+int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, const int32_t *topk_idx,
+            const float *topk_w, const hla_bf16 *W_gate, const hla_bf16 *W_up,
+            const hla_bf16 *W_down, const hla_bf16 *Ws_gate, const hla_bf16 *Ws_up,
+            const hla_bf16 *Ws_down, const hla_bf16 *residual, hla_bf16 *y, void *ws,
+            cudaStream_t st, cudaStream_t pf) {
+    const MoeLayout L = moe_layout(M, Hd, I, E, k, nsh);
+    char *w = reinterpret_cast<char *>(ws);
+    MoeArgs a;
+    a.M = M; a.Hd = Hd; a.I = I; a.E = E; a.k = k; a.nsh = nsh; a.P = L.P; a.KS = L.KS; a.TT = L.TT;
+    a.x = x; a.topk_idx = topk_idx; a.topk_w = topk_w;
+    a.W_gate = W_gate; a.W_up = W_up; a.W_down = W_down;
+    a.Ws_gate = Ws_gate; a.Ws_up = Ws_up; a.Ws_down = Ws_down;
+    a.residual = residual; a.y = y;
+    a.meta = reinterpret_cast<int *>(w + L.off_meta);
+    a.unit_expert = reinterpret_cast<int *>(w + L.off_unit_expert);
+    a.unit_off = reinterpret_cast<int *>(w + L.off_unit_off);
+    a.item_gu = reinterpret_cast<int *>(w + L.off_item_gu);
+    a.item_dn = reinterpret_cast<int *>(w + L.off_item_dn);
+    a.pos_token = reinterpret_cast<int *>(w + L.off_pos_token);
+    a.pos_slot = reinterpret_cast<int *>(w + L.off_pos_slot);
+    a.h = reinterpret_cast<uint16_t *>(w + L.off_h);
+    a.part_g = reinterpret_cast<float *>(w + L.off_part_g);
+    a.part_u = reinterpret_cast<float *>(w + L.off_part_u);
+    a.ypart = reinterpret_cast<float *>(w + L.off_ypart);
+
+    const bool side = pf != nullptr && nsh > 0;
+    if (side) {
+        if (!g_moe_events.ok()) return HLA_ERR_CUDA;
+        if (cudaEventRecord(g_moe_events.fork, st) != cudaSuccess) return HLA_ERR_CUDA;
+        if (cudaStreamWaitEvent(pf, g_moe_events.fork, 0) != cudaSuccess) return HLA_ERR_CUDA;
+        const size_t mat = (size_t)nsh * I * Hd * sizeof(uint16_t);
+        int r = run_l2_prefetch(Ws_gate, mat, pf);
+        if (r == HLA_OK) r = run_l2_prefetch(Ws_up, mat, pf);
+        if (r == HLA_OK) r = run_l2_prefetch(Ws_down, mat, pf);
+        if (r != HLA_OK) return r;
+        if (cudaEventRecord(g_moe_events.join, pf) != cudaSuccess) return HLA_ERR_CUDA;
+    }
+
+    moe_dispatch_kernel<<<1, kDispatchThreads, 0, st>>>(a);
+    int r = launch_status();
+    if (r != HLA_OK) return r;
+    trace_before(kTraceMoeGateup, st);
+    if (L.TT == 8) {
+        static int g1 = 0;
+        if (!g1) g1 = persistent_grid(moe_gateup_kernel<1>);
+        moe_gateup_kernel<1><<<g1, kMoeThreads, 0, st>>>(a);
+    } else {
+        static int g2 = 0;
+        if (!g2) g2 = persistent_grid(moe_gateup_kernel<2>);
+        moe_gateup_kernel<2><<<g2, kMoeThreads, 0, st>>>(a);
+    }
+    trace_after(kTraceMoeGateup, st);
+    if ((r = launch_status()) != HLA_OK) return r;
+    if (L.KS > 1) {
+        moe_swiglu_reduce_kernel<<<4 * sm_count(), 256, 0, st>>>(a);
+        if ((r = launch_status()) != HLA_OK) return r;
+    }
+    trace_before(kTraceMoeDown, st);
+    if (L.TT == 8) {
+        static int d1 = 0;
+        if (!d1) d1 = persistent_grid(moe_down_kernel<1>);
+        moe_down_kernel<1><<<d1, kMoeThreads, 0, st>>>(a);
+    } else {
+        static int d2 = 0;
+        if (!d2) d2 = persistent_grid(moe_down_kernel<2>);
+        moe_down_kernel<2><<<d2, kMoeThreads, 0, st>>>(a);
+    }
+    trace_after(kTraceMoeDown, st);
+    if ((r = launch_status()) != HLA_OK) return r;
+    const dim3 cgrid((unsigned)((Hd / 4 + 127) / 128), (unsigned)M);
+    moe_combine_kernel<<<cgrid, 128, 0, st>>>(a);
+    if ((r = launch_status()) != HLA_OK) return r;
+    if (side && cudaStreamWaitEvent(st, g_moe_events.join, 0) != cudaSuccess) return HLA_ERR_CUDA;
+    set_variant("moe<tt%d,ks%d%s>", L.TT, L.KS, side ? ",prefetch" : "");
+    return HLA_OK;
+}
+
+}  // namespace hla
+
+using namespace hla;
+
+extern "C" size_t moe_expert_forward_workspace_size(int M, int Hd, int I, int E, int k,
+                                                    int n_shared) {
+    if (M < 1 || Hd < 32 || I < 32 || E < 1 || k < 1 || n_shared < 0) return 0;
+    return moe_workspace_bytes(M, Hd, I, E, k, n_shared);
+}
+
+extern "C" int moe_expert_forward(int M, int Hd, int I, int E, int k, int n_shared,
+                                  const hla_bf16 *x, const int32_t *topk_idx, const float *topk_w,
+                                  const hla_bf16 *W_gate, const hla_bf16 *W_up,
+                                  const hla_bf16 *W_down, const hla_bf16 *Ws_gate,
+                                  const hla_bf16 *Ws_up, const hla_bf16 *Ws_down,
+                                  const hla_bf16 *residual, hla_bf16 *y, void *ws,
+                                  size_t ws_bytes, hla_stream stream, hla_stream prefetch_stream) {
+    HLA_REQUIRE(M >= 1 && Hd >= 32 && I >= 32 && E >= 1 && k >= 1 && n_shared >= 0,
+                HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(M <= 256 && k <= 16 && k <= E && E + n_shared <= 1024 && n_shared <= 16 &&
+                    Hd % 32 == 0 && I % 32 == 0,
+                HLA_ERR_UNSUPPORTED);
+    HLA_REQUIRE(x && topk_idx && topk_w && W_gate && W_up && W_down && y, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(n_shared == 0 || (Ws_gate && Ws_up && Ws_down), HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(aligned16(x) && aligned16(topk_idx) && aligned16(topk_w) && aligned16(W_gate) &&
+                    aligned16(W_up) && aligned16(W_down) && aligned16(y) &&
+                    (!residual || aligned16(residual)) &&
+                    (n_shared == 0 || (aligned16(Ws_gate) && aligned16(Ws_up) && aligned16(Ws_down))),
+                HLA_ERR_MISALIGNED);
+    const size_t need = moe_workspace_bytes(M, Hd, I, E, k, n_shared);
+    HLA_REQUIRE(ws && ws_bytes >= need, HLA_ERR_WORKSPACE);
+    HLA_REQUIRE(aligned16(ws), HLA_ERR_MISALIGNED);
+    return run_moe(M, Hd, I, E, k, n_shared, x, topk_idx, topk_w, W_gate, W_up, W_down, Ws_gate,
+                   Ws_up, Ws_down, residual, y, ws, (cudaStream_t)stream,
+                   (cudaStream_t)prefetch_stream);
+}

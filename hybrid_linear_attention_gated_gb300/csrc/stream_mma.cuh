@@ -1,0 +1,96 @@
+// Warp-level weight-streaming tile for skinny products out[n, r] = sum_k W[r, k] x[n, k].
+//
+// At decode batch sizes the weights (16 rows per warp here) are read exactly once
+// and each weight element meets only a handful of tokens, so the product is bound
+// by how fast the weights stream from HBM ("moving expert weights through GPU
+// memory was a major constraint", "Kimi K3: From Day-0 Availability to Optimized
+// Inference").  The tile keeps the weight stream as wide as possible: every lane
+// issues 128-bit loads straight into mma.sync A fragments, several K steps ahead.
+//
+// Fragment trick: m16n8k16 expects lane (g, t) (g = lane/4, t = lane%4) to hold
+// A[g][2t,2t+1], A[g+8][2t,2t+1], A[g][2t+8,2t+9], A[g+8][2t+8,2t+9] and
+// B[2t,2t+1][g], B[2t+8,2t+9][g].  A dot product does not care about the order of
+// its K terms, so lane (g, t) instead loads 8 consecutive K values (16 bytes)
+// k0+8t .. k0+8t+7 of weight rows g and g+8 and of token row g, and feeds them to
+// two MMAs: physical (8t, 8t+1 | 8t+2, 8t+3) as logical (2t, 2t+1 | 2t+8, 2t+9) of
+// the first MMA and (8t+4, 8t+5 | 8t+6, 8t+7) of the second.  A and B use the same
+// permutation, so the products are exact dot products over 32 K values per pair.
+#pragma once
+
+#include "common.cuh"
+
+namespace hla {
+
+// Accumulate, for one warp, acc[m][nt] += W_m[16 rows] . X[8 tokens of tile nt]^T over
+// K in [kb, ke) (multiples of 32).  wg[m] / wg8[m] point at weight rows g and g+8 of
+// matrix m (element 0 of the row); xr[nt] points at the token row that lane group g
+// feeds to tile nt.  Lanes whose rows / tokens fall outside the problem point at any
+// valid row; their outputs are simply not stored.
+template <int NMAT, int NT, int UNROLL>
+__device__ __forceinline__ void warp_stream_tile(const uint16_t *const (&wg)[NMAT],
+                                                 const uint16_t *const (&wg8)[NMAT],
+                                                 const uint16_t *const (&xr)[NT], int kb, int ke,
+                                                 float (&acc)[NMAT][NT][4]) {
+    const int t8 = (threadIdx.x & 3) * 8;
+    const int nsteps = (ke - kb) >> 5;
+    uint4 wa[UNROLL][NMAT][2];
+    uint4 xb[UNROLL][NT];
+
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+        if (u < nsteps) {
+            const int k = kb + 32 * u + t8;
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+                wa[u][m][0] = ld_weight_v4(wg[m] + k);
+                wa[u][m][1] = ld_weight_v4(wg8[m] + k);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) xb[u][nt] = ld_act_v4(xr[nt] + k);
+        }
+    }
+
+    for (int s0 = 0; s0 < nsteps; s0 += UNROLL) {
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int s = s0 + u;
+            if (s < nsteps) {
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_bf16_16816(acc[m][nt], wa[u][m][0].x, wa[u][m][1].x, wa[u][m][0].y,
+                                       wa[u][m][1].y, xb[u][nt].x, xb[u][nt].y);
+                        mma_bf16_16816(acc[m][nt], wa[u][m][0].z, wa[u][m][1].z, wa[u][m][0].w,
+                                       wa[u][m][1].w, xb[u][nt].z, xb[u][nt].w);
+                    }
+                }
+                if (s + UNROLL < nsteps) {
+                    const int k = kb + 32 * (s + UNROLL) + t8;
+#pragma unroll
+                    for (int m = 0; m < NMAT; ++m) {
+                        wa[u][m][0] = ld_weight_v4(wg[m] + k);
+                        wa[u][m][1] = ld_weight_v4(wg8[m] + k);
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) xb[u][nt] = ld_act_v4(xr[nt] + k);
+                }
+            }
+        }
+    }
+}
+
+// Output coordinates of accumulator element e (0..3) of tile nt for this lane:
+// row (within the 16-row block) and token (within the 8*NT token group).
+__device__ __forceinline__ int acc_row(int e) { return (threadIdx.x & 31) / 4 + ((e & 2) ? 8 : 0); }
+__device__ __forceinline__ int acc_tok(int nt, int e) { return nt * 8 + (threadIdx.x & 3) * 2 + (e & 1); }
+
+// Split [0, K) into `split` slices that are multiples of 32 and return slice ks.
+__device__ __forceinline__ void k_slice(int K, int split, int ks, int &kb, int &ke) {
+    const int steps = K >> 5;
+    const int per = (steps + split - 1) / split;
+    kb = min(steps, ks * per) * 32;
+    ke = min(steps, (ks + 1) * per) * 32;
+}
+
+}  // namespace hla

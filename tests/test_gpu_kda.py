@@ -1,0 +1,194 @@
+"""KDA decode step, speculative verify / accept / replay on the GPU against the oracle."""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hybrid_linear_attention_gated_gb300 import hla, inputs
+from tests.gpu_common import KDA_MAX_REL, f64, max_rel, require_gpu, warm_states
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_gpu()
+
+
+def _to(d, dev):
+    return {k: v.to(dev) for k, v in d.items()}
+
+
+def _decode(dev, S, inp, o_dtype=hla.HLA_F32, state_idx=None):
+    B, H, d = inp["q"].shape
+    o = torch.empty(B, H, d, device=dev, dtype=torch.float32 if o_dtype == hla.HLA_F32 else torch.bfloat16)
+    hla.kda_decode_step(B, H, d, d, S, state_idx, inp["q"], inp["k"], inp["v"], inp["alpha"],
+                        inp["beta"], o, o_dtype)
+    return o
+
+
+def _np(inp):
+    return {k: f64(v) for k, v in inp.items()}
+
+
+def test_tiny_case_steps_verify_accept_replay(dev):
+    """Batch 1, 4 heads, d=64: 8 steps from S0 ~ N(0,0.02), a 4-token draft, 2 accepted."""
+    g = inputs.generator(0)
+    B, H, d, T = 1, 4, 64, 4
+    S0 = inputs.small_state(B, H, d, d, g)
+    steps = [inputs.kda_inputs((B,), H, d, d, g) for _ in range(8)]
+    win = inputs.kda_inputs((B, T), H, d, d, g)
+    draft, target, a_int = inputs.accept_ids(B, T, g)
+    # the tiny case fixes 2 accepted tokens
+    target = draft.clone()
+    target[:, 2] = draft[:, 2] + 1
+
+    S = S0.to(dev)
+    S_ref = f64(S0)
+    for st in steps:
+        o = _decode(dev, S, _to(st, dev))
+        n = _np(st)
+        S_ref, o_ref = oracle.kda.kda_step(S_ref, n["q"], n["k"], n["v"], n["alpha"], n["beta"])
+        assert max_rel(f64(o), o_ref) < KDA_MAX_REL
+    assert max_rel(f64(S), S_ref) < KDA_MAX_REL
+
+    wd, wn = _to(win, dev), _np(win)
+    S_before = S.clone()
+    ov = torch.empty(B, T, H, d, device=dev)
+    hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, S, None, wd["q"], wd["k"], wd["v"],
+                               wd["alpha"], wd["beta"], None, ov)
+    acc = torch.zeros(B, dtype=torch.int32, device=dev)
+    com = torch.full((B,), 9, dtype=torch.int32, device=dev)
+    hla.spec_accept_prefix(B, T, draft.to(dev), target.to(dev), acc, com)
+    hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, S, None, wd["q"], wd["k"],
+                               wd["v"], wd["alpha"], wd["beta"], acc, None)
+    torch.cuda.synchronize()
+    ov_ref = oracle.kda.spec_verify(S_ref, wn["q"], wn["k"], wn["v"], wn["alpha"], wn["beta"])
+    a_ref, com_ref = oracle.kda.accept_prefix(draft.numpy(), target.numpy(), np.array([9]))
+    S_new_ref = oracle.kda.spec_replay(S_ref, wn["q"], wn["k"], wn["v"], wn["alpha"], wn["beta"], a_ref)
+    assert int(a_ref[0]) == 2
+    assert np.array_equal(acc.cpu().numpy(), a_ref) and np.array_equal(com.cpu().numpy(), com_ref)
+    assert max_rel(f64(ov), ov_ref) < KDA_MAX_REL
+    assert max_rel(f64(S), S_new_ref) < KDA_MAX_REL
+    assert not torch.equal(S, S_before)
+
+
+@pytest.mark.parametrize("B", [1, 2, 8, 32, 64])
+def test_decode_step_sweep(dev, B):
+    """Batch sweep at H=32, d=128 from warm committed states (256 prior updates)."""
+    H, d = 32, 128
+    S0 = warm_states(1, B, H, d)
+    inp = inputs.kda_inputs((B,), H, d, d, inputs.generator(1000 + B))
+    S = S0.to(dev)
+    o = _decode(dev, S, _to(inp, dev))
+    torch.cuda.synchronize()
+    n = _np(inp)
+    S_ref, o_ref = oracle.kda.kda_step(f64(S0), n["q"], n["k"], n["v"], n["alpha"], n["beta"])
+    assert max_rel(f64(o), o_ref) < KDA_MAX_REL
+    assert max_rel(f64(S), S_ref) < KDA_MAX_REL
+    assert hla.hla_last_variant().startswith("kda_recur<dk128")
+
+
+def test_decode_bf16_output_and_state_idx(dev):
+    B, H, d = 8, 32, 128
+    S0 = warm_states(1, B, H, d)
+    inp = inputs.kda_inputs((B,), H, d, d, inputs.generator(77))
+    perm = torch.randperm(12, generator=inputs.generator(78))[:B].to(torch.int32)
+    pool = torch.zeros(12, H, d, d)
+    pool[perm.long()] = S0
+    Sd = pool.to(dev)
+    o = _decode(dev, Sd, _to(inp, dev), hla.HLA_BF16, perm.to(dev))
+    torch.cuda.synchronize()
+    n = _np(inp)
+    S_ref, o_ref = oracle.kda.kda_step(f64(S0), n["q"], n["k"], n["v"], n["alpha"], n["beta"])
+    # bf16 output: rounding of 2^-9 relative on top of the fp32 path
+    assert max_rel(f64(o), o_ref) < 5e-3
+    got = Sd.cpu()
+    assert max_rel(got[perm.long()].double().numpy(), S_ref) < KDA_MAX_REL
+    untouched = torch.ones(12, dtype=torch.bool)
+    untouched[perm.long()] = False
+    assert torch.count_nonzero(got[untouched]) == 0
+
+
+def test_spec_window_config(dev):
+    """B=16, T=4, H=32, d=128, accepted length uniform in {0..4}."""
+    B, T, H, d = 16, 4, 32, 128
+    S0 = warm_states(2, B, H, d)
+    g = inputs.generator(2)
+    win = inputs.kda_inputs((B, T), H, d, d, g)
+    draft, target, a_int = inputs.accept_ids(B, T, g)
+    S = S0.to(dev)
+    wd, wn = _to(win, dev), _np(win)
+    ov = torch.empty(B, T, H, d, device=dev)
+    hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, S, None, wd["q"], wd["k"], wd["v"],
+                               wd["alpha"], wd["beta"], None, ov)
+    torch.cuda.synchronize()
+    assert torch.equal(S.cpu(), S0), "verify must not write the committed state"
+    acc = torch.zeros(B, dtype=torch.int32, device=dev)
+    com = torch.arange(B, dtype=torch.int32, device=dev)
+    hla.spec_accept_prefix(B, T, draft.to(dev), target.to(dev), acc, com)
+    hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, S, None, wd["q"], wd["k"],
+                               wd["v"], wd["alpha"], wd["beta"], acc, None)
+    torch.cuda.synchronize()
+    a_ref, com_ref = oracle.kda.accept_prefix(draft.numpy(), target.numpy(), np.arange(B))
+    assert np.array_equal(a_ref, a_int.numpy())
+    assert np.array_equal(acc.cpu().numpy(), a_ref)
+    assert np.array_equal(com.cpu().numpy(), com_ref)
+    ov_ref = oracle.kda.spec_verify(f64(S0), wn["q"], wn["k"], wn["v"], wn["alpha"], wn["beta"])
+    S_ref = oracle.kda.spec_replay(f64(S0), wn["q"], wn["k"], wn["v"], wn["alpha"], wn["beta"], a_ref)
+    assert max_rel(f64(ov), ov_ref) < KDA_MAX_REL
+    Sg = S.cpu()
+    assert max_rel(Sg.double().numpy(), S_ref) < KDA_MAX_REL
+    for b in range(B):  # nothing accepted -> state bitwise untouched
+        if a_ref[b] == 0:
+            assert torch.equal(Sg[b], S0[b])
+
+
+def test_replay_all_equals_decode_steps_bitwise(dev):
+    B, T, H, d = 4, 4, 32, 128
+    S0 = warm_states(3, B, H, d)
+    win = inputs.kda_inputs((B, T), H, d, d, inputs.generator(31))
+    wd = _to(win, dev)
+    S1 = S0.to(dev)
+    acc = torch.full((B,), T, dtype=torch.int32, device=dev)
+    hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, S1, None, wd["q"], wd["k"], wd["v"],
+                               wd["alpha"], wd["beta"], acc, None)
+    S2 = S0.to(dev)
+    for t in range(T):
+        step = {k: v[:, t].contiguous() for k, v in wd.items()}
+        _decode(dev, S2, step)
+    torch.cuda.synchronize()
+    assert torch.equal(S1, S2)
+
+
+@pytest.mark.parametrize("cw", ["16", "32", "64", "128"])
+def test_slice_width_variants_bitwise_equal(dev, cw, monkeypatch):
+    B, H, d = 2, 32, 128
+    S0 = warm_states(1, B, H, d)
+    inp = _to(inputs.kda_inputs((B,), H, d, d, inputs.generator(5)), dev)
+    S_ref = S0.to(dev)
+    o_ref = _decode(dev, S_ref, inp)
+    monkeypatch.setenv("HLA_KDA_CW", cw)
+    S = S0.to(dev)
+    o = _decode(dev, S, inp)
+    torch.cuda.synchronize()
+    assert hla.hla_last_variant() == f"kda_recur<dk128,cw{cw},decode>"
+    assert torch.equal(S, S_ref) and torch.equal(o, o_ref)
+
+
+def test_run_to_run_determinism(dev):
+    B, H, d = 16, 32, 128
+    S0 = warm_states(2, B, H, d)
+    win = _to(inputs.kda_inputs((B, 4), H, d, d, inputs.generator(9)), dev)
+    outs = []
+    for _ in range(2):
+        S = S0.to(dev)
+        ov = torch.empty(B, 4, H, d, device=dev)
+        hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, 4, H, d, d, S, None, win["q"], win["k"],
+                                   win["v"], win["alpha"], win["beta"], None, ov)
+        outs.append(ov)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])

@@ -1,0 +1,104 @@
+"""The full hybrid decode layer (hidden 7168, 32 KDA heads of 128, 256 experts top-8 + 1
+shared) through the C-ABI executor, against the oracle's composed layer on sampled
+sequences (each sequence's layer output depends only on its own token and state)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hybrid_linear_attention_gated_gb300 import hla, inputs
+from tests.gpu_common import (FULL, LAYER_FROB_REL, ExpertCache, f64, frob_rel, require_gpu,
+                              warm_states)
+
+pytestmark = pytest.mark.gpu
+
+H, D = 32, 128
+ROUTER_MARGIN = 1e-3   # skip sampled tokens whose oracle top-(k+1) logits are closer than this
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_gpu()
+
+
+@pytest.fixture(scope="module")
+def layer(dev, full_moe):
+    w = inputs.layer_weights(FULL["Hd"], H, D, D, inputs.generator(4, dev), device=dev)
+    w.update({k: full_moe[k] for k in ("W_r", "W_gate", "W_up", "W_down", "Ws_gate", "Ws_up", "Ws_down")})
+    L = hla.make_layer(FULL["Hd"], H, D, D, FULL["E"], FULL["k"], FULL["I"], FULL["n_shared"], 1e-6, w)
+    p = dict(H=H, dk=D, dv=D, top_k=FULL["k"], eps=1e-6, gamma_attn=f64(w["gamma_attn"]),
+             gamma_moe=f64(w["gamma_moe"]), W_qkvgb=f64(w["W_qkvgb"]), W_o=f64(w["W_o"]),
+             W_r=full_moe["W_r64"])
+    return w, L, p
+
+
+def _run(dev, L, M, x, S, prefetch=False):
+    y = torch.empty(M, FULL["Hd"], dtype=torch.bfloat16, device=dev)
+    nb = hla.hla_decode_layer_workspace_size(L, M)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream() if prefetch else 0
+    hla.hla_decode_layer(L, M, x, S, None, y, ws, nb, prefetch_stream=side)
+    return y
+
+
+@pytest.mark.parametrize("M", [1, 8, 64])
+def test_decode_layer(dev, full_moe, layer, M):
+    w, L, p = layer
+    x = inputs.activations(M, FULL["Hd"], inputs.generator(4000 + M))
+    S0 = warm_states(4, M, H, D)
+    S = S0.to(dev)
+    y = _run(dev, L, M, x.to(dev), S)
+    torch.cuda.synchronize()
+    assert hla.hla_last_variant() == "decode_layer"
+    cache = ExpertCache(full_moe)
+    checked = 0
+    for m in sorted(set([0, M // 2, M - 1, 1 % M, (M * 3) // 4])):
+        y_ref, S_ref, aux = oracle.layer.decode_layer(f64(x)[m:m + 1], f64(S0)[m:m + 1], p, cache,
+                                                       cache.shared())
+        top = np.sort(aux["logits"][0])[::-1][:FULL["k"] + 1]
+        if np.any(-np.diff(top) < ROUTER_MARGIN):
+            continue  # a near tie in routing: the two sides may legitimately pick differently
+        assert frob_rel(f64(y)[m:m + 1], y_ref) < LAYER_FROB_REL, m
+        assert frob_rel(f64(S)[m:m + 1], S_ref) < LAYER_FROB_REL, m
+        checked += 1
+        if checked == 3:
+            break
+    assert checked >= 1
+
+
+def test_layer_prefetch_is_bitwise_neutral(dev, layer):
+    w, L, p = layer
+    M = 8
+    x = inputs.activations(M, FULL["Hd"], inputs.generator(4100)).to(dev)
+    S0 = warm_states(4, M, H, D)
+    S1, S2 = S0.to(dev), S0.to(dev)
+    y1 = _run(dev, L, M, x, S1)
+    y2 = _run(dev, L, M, x, S2, prefetch=True)
+    torch.cuda.synchronize()
+    assert hla.hla_last_variant() == "decode_layer<prefetch>"
+    assert torch.equal(y1, y2) and torch.equal(S1, S2)
+
+
+def test_layer_in_cuda_graph_matches_eager(dev, layer):
+    w, L, p = layer
+    M = 8
+    x = inputs.activations(M, FULL["Hd"], inputs.generator(4200)).to(dev)
+    S0 = warm_states(4, M, H, D)
+    S_eager = S0.to(dev)
+    y_eager = _run(dev, L, M, x, S_eager)
+    S_graph = S0.to(dev)
+    y = torch.empty(M, FULL["Hd"], dtype=torch.bfloat16, device=dev)
+    nb = hla.hla_decode_layer_workspace_size(L, M)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            hla.hla_decode_layer(L, M, x, S_graph, None, y, ws, nb, prefetch_stream=side)
+    S_graph.copy_(S0.to(dev))
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_eager) and torch.equal(S_graph, S_eager)

@@ -1,0 +1,204 @@
+"""Skinny projections, RMSNorm, router top-k and routed + shared experts on the GPU vs the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hybrid_linear_attention_gated_gb300 import hla, inputs
+from tests.gpu_common import (FULL, MOE_FROB_REL, PROJ_FROB_REL_BF16, PROJ_FROB_REL_F32,
+                              ROUTER_W_REL, ExpertCache, f64, frob_rel, max_rel, require_gpu)
+
+pytestmark = pytest.mark.gpu
+
+TIE_GAP = 1e-5  # minimum gap between adjacent top-(k+1) sigmoid scores of a test token
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_gpu()
+
+
+def _ws(nbytes, dev):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+
+
+def tie_free_activations(M, Hd, W_r64, k, seed, device="cpu"):
+    """x ~ N(0,1) bf16 [M, Hd]; a token whose top-(k+1) oracle scores come within TIE_GAP of
+    each other is redrawn from the next sub-seed.  Returns (x, number of redraws)."""
+    rows, redraws = [], 0
+    for m in range(M):
+        sub = 0
+        while True:
+            x = inputs.activations(1, Hd, inputs.generator(seed * 1000 + m * 97 + sub))
+            s = np.sort(oracle.numerics.sigmoid(f64(x) @ W_r64.T)[0])[::-1][:k + 1]
+            if np.all(-np.diff(s) >= TIE_GAP):
+                break
+            sub += 1
+            redraws += 1
+        rows.append(x)
+    return torch.cat(rows).to(device), redraws
+
+
+# ----------------------------------------------------------------------------- projections
+
+@pytest.mark.parametrize("M,N,K,split,res,out", [
+    (1, 7168, 4096, 0, True, hla.HLA_BF16), (2, 256, 7168, 0, False, hla.HLA_F32),
+    (3, 1028, 256, 1, False, hla.HLA_F32), (13, 1000, 512, 3, True, hla.HLA_BF16),
+    (64, 7168, 4096, 0, True, hla.HLA_BF16), (64, 2048, 7168, 2, False, hla.HLA_F32),
+    (256, 96, 256, 0, False, hla.HLA_F32), (9, 16, 32, 1, True, hla.HLA_F32)])
+def test_skinny_proj(dev, M, N, K, split, res, out):
+    g = inputs.generator(M * 7 + N)
+    x = inputs.activations(M, K, g)
+    W = inputs.weight((N, K), g)
+    r = inputs.activations(M, N, g) if res else None
+    y = torch.empty(M, N, device=dev, dtype=torch.bfloat16 if out == hla.HLA_BF16 else torch.float32)
+    nb = hla.skinny_proj_splitk_workspace_size(M, N, K, split)
+    ws = _ws(nb, dev)
+    hla.skinny_proj_splitk(M, N, K, x.to(dev), W.to(dev), r.to(dev) if res else None, y, out, split,
+                           ws, ws.numel())
+    torch.cuda.synchronize()
+    ref = oracle.moe.linear(f64(x), f64(W)) + (f64(r) if res else 0.0)
+    tol = PROJ_FROB_REL_BF16 if out == hla.HLA_BF16 else PROJ_FROB_REL_F32
+    assert frob_rel(f64(y), ref) < tol
+
+
+def test_split_counts_agree(dev):
+    M, N, K = 4, 512, 2048
+    g = inputs.generator(3)
+    x, W = inputs.activations(M, K, g).to(dev), inputs.weight((N, K), g).to(dev)
+    outs = []
+    for split in (1, 2, 5, 16):
+        y = torch.empty(M, N, device=dev)
+        ws = _ws(hla.skinny_proj_splitk_workspace_size(M, N, K, split), dev)
+        hla.skinny_proj_splitk(M, N, K, x, W, None, y, hla.HLA_F32, split, ws, ws.numel())
+        outs.append(y)
+    torch.cuda.synchronize()
+    for y in outs[1:]:
+        assert frob_rel(f64(y), f64(outs[0])) < 1e-5
+
+
+@pytest.mark.parametrize("M,Hd,H,d", [(1, 256, 4, 64), (5, 512, 2, 128), (64, 1024, 4, 128)])
+def test_qkvg_projection(dev, M, Hd, H, d):
+    g = inputs.generator(M + Hd)
+    x = inputs.activations(M, Hd, g)
+    W = inputs.weight((4 * H * d + H, Hd), g, std=0.05)
+    outs = dict(q=torch.empty(M, H, d, dtype=torch.bfloat16, device=dev),
+                k=torch.empty(M, H, d, dtype=torch.bfloat16, device=dev),
+                v=torch.empty(M, H, d, dtype=torch.bfloat16, device=dev),
+                alpha=torch.empty(M, H, d, device=dev), beta=torch.empty(M, H, device=dev))
+    ws = _ws(hla.kda_qkvg_proj_workspace_size(M, Hd, H, d, d, 0), dev)
+    hla.kda_qkvg_proj(M, Hd, H, d, d, x.to(dev), W.to(dev), outs["q"], outs["k"], outs["v"],
+                      outs["alpha"], outs["beta"], 0, ws, ws.numel())
+    torch.cuda.synchronize()
+    q, k, v, al, be = oracle.layer.qkvg_epilogue(oracle.moe.linear(f64(x), f64(W)), H, d, d)
+    # bf16 outputs: both sides round to bf16, so they may differ by one bf16 ulp (2^-8 rel)
+    for name, ref in (("q", q), ("k", k), ("v", v)):
+        assert max_rel(f64(outs[name]), ref) < 1e-2, name
+        assert frob_rel(f64(outs[name]), ref) < 4e-3, name
+    assert max_rel(f64(outs["alpha"]), al) < 1e-4
+    assert max_rel(f64(outs["beta"]), be) < 1e-4
+
+
+@pytest.mark.parametrize("M,Hd", [(1, 7168), (64, 7168), (3, 256)])
+def test_rmsnorm(dev, M, Hd):
+    g = inputs.generator(M + 5)
+    x, gam = inputs.activations(M, Hd, g), inputs.gains(Hd, g)
+    y = torch.empty(M, Hd, dtype=torch.bfloat16, device=dev)
+    hla.hla_rmsnorm(M, Hd, x.to(dev), gam.to(dev), 1e-6, y)
+    torch.cuda.synchronize()
+    ref = oracle.moe.rmsnorm(f64(x), f64(gam), 1e-6)
+    assert max_rel(f64(y), ref) < 1e-2 and frob_rel(f64(y), ref) < 4e-3
+
+
+# ----------------------------------------------------------------------------- tiny MoE
+
+@pytest.mark.parametrize("n_shared", [0, 1])
+def test_tiny_moe(dev, n_shared):
+    """16 experts, top-2, hidden 256, intermediate 128, one token, seed 0."""
+    M, Hd, I, E, k = 1, 256, 128, 16, 2
+    g = inputs.generator(0)
+    w = inputs.moe_weights(E, Hd, I, n_shared, g)
+    x, redraws = tie_free_activations(M, Hd, f64(w["W_r"]), k, 0)
+    wd = {kk: (vv.to(dev) if vv is not None else None) for kk, vv in w.items()}
+    idx = torch.empty(M, k, dtype=torch.int32, device=dev)
+    wt = torch.empty(M, k, device=dev)
+    logits = torch.empty(M, E, device=dev)
+    ws = _ws(hla.moe_route_topk_workspace_size(M, Hd, E), dev)
+    hla.moe_route_topk(M, Hd, E, k, x.to(dev), wd["W_r"], idx, wt, logits, ws, ws.numel())
+    y = torch.empty(M, Hd, dtype=torch.bfloat16, device=dev)
+    nb = hla.moe_expert_forward_workspace_size(M, Hd, I, E, k, n_shared)
+    ws2 = _ws(nb, dev)
+    hla.moe_expert_forward(M, Hd, I, E, k, n_shared, x.to(dev), idx, wt, wd["W_gate"], wd["W_up"],
+                           wd["W_down"], wd["Ws_gate"], wd["Ws_up"], wd["Ws_down"], None, y, ws2, nb)
+    torch.cuda.synchronize()
+    idx_ref, w_ref, lg_ref = oracle.moe.route_topk(f64(x), f64(w["W_r"]), k)
+    assert np.array_equal(idx.cpu().numpy(), idx_ref)
+    assert max_rel(f64(wt), w_ref) < ROUTER_W_REL
+    assert frob_rel(f64(logits), lg_ref) < 1e-5
+    shared = [(f64(w["Ws_gate"][0]), f64(w["Ws_up"][0]), f64(w["Ws_down"][0]))] if n_shared else []
+    y_ref = oracle.moe.moe_forward(f64(x), idx_ref, w_ref,
+                                   (f64(w["W_gate"]), f64(w["W_up"]), f64(w["W_down"])), shared)
+    assert frob_rel(f64(y), y_ref) < MOE_FROB_REL
+
+
+# ----------------------------------------------------------------------------- full-size MoE
+
+def _run_moe(dev, w, x, idx, wt, residual=None, prefetch=False):
+    M = x.shape[0]
+    Hd, I, E, k, ns = FULL["Hd"], FULL["I"], FULL["E"], FULL["k"], FULL["n_shared"]
+    y = torch.empty(M, Hd, dtype=torch.bfloat16, device=dev)
+    nb = hla.moe_expert_forward_workspace_size(M, Hd, I, E, k, ns)
+    ws = _ws(nb, dev)
+    side = torch.cuda.Stream() if prefetch else 0
+    hla.moe_expert_forward(M, Hd, I, E, k, ns, x, idx, wt, w["W_gate"], w["W_up"], w["W_down"],
+                           w["Ws_gate"], w["Ws_up"], w["Ws_down"], residual, y, ws, nb,
+                           prefetch_stream=side)
+    return y
+
+
+@pytest.mark.parametrize("M", [1, 2, 8, 32, 64])
+def test_full_moe(dev, full_moe, M):
+    Hd, E, k = FULL["Hd"], FULL["E"], FULL["k"]
+    x, _ = tie_free_activations(M, Hd, full_moe["W_r64"], k, 3 + M)
+    xd = x.to(dev)
+    idx = torch.empty(M, k, dtype=torch.int32, device=dev)
+    wt = torch.empty(M, k, device=dev)
+    logits = torch.empty(M, E, device=dev)
+    ws = _ws(hla.moe_route_topk_workspace_size(M, Hd, E), dev)
+    hla.moe_route_topk(M, Hd, E, k, xd, full_moe["W_r"], idx, wt, logits, ws, ws.numel())
+    res = inputs.activations(M, Hd, inputs.generator(55 + M)).to(dev)
+    y = _run_moe(dev, full_moe, xd, idx, wt, residual=res)
+    torch.cuda.synchronize()
+    idx_ref, w_ref, lg_ref = oracle.moe.route_topk(f64(x), full_moe["W_r64"], k)
+    assert np.array_equal(idx.cpu().numpy(), idx_ref)       # every token, bit-exact
+    assert max_rel(f64(wt), w_ref) < ROUTER_W_REL
+    assert frob_rel(f64(logits), lg_ref) < 1e-5
+    cache = ExpertCache(full_moe)
+    sample = sorted(set([0, M // 2, M - 1]))
+    y_ref = oracle.moe.moe_forward(f64(x)[sample], idx_ref[sample], w_ref[sample], cache,
+                                   cache.shared(), residual=f64(res)[sample])
+    assert frob_rel(f64(y)[sample], y_ref) < MOE_FROB_REL
+
+
+def test_skewed_routing_and_prefetch_bitwise(dev, full_moe):
+    """All 64 tokens on the same 8 experts (64 tokens per expert: several token groups per
+    weight row block); prefetch on and off must give bit-identical results."""
+    M, Hd, k = 64, FULL["Hd"], FULL["k"]
+    g = inputs.generator(99)
+    x = inputs.activations(M, Hd, g)
+    experts = torch.tensor([5, 17, 42, 99, 128, 200, 230, 255], dtype=torch.int32)
+    idx = experts.repeat(M, 1)
+    raw = torch.rand(M, k, generator=g) + 0.1
+    wt = raw / raw.sum(1, keepdim=True)
+    xd = x.to(dev)
+    y1 = _run_moe(dev, full_moe, xd, idx.to(dev), wt.to(dev))
+    y2 = _run_moe(dev, full_moe, xd, idx.to(dev), wt.to(dev), prefetch=True)
+    y3 = _run_moe(dev, full_moe, xd, idx.to(dev), wt.to(dev))
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(y1, y3)
+    cache = ExpertCache(full_moe)
+    sample = [0, 31, 63]
+    y_ref = oracle.moe.moe_forward(f64(x)[sample], idx.numpy()[sample], f64(wt)[sample], cache,
+                                   cache.shared())
+    assert frob_rel(f64(y1)[sample], y_ref) < MOE_FROB_REL
