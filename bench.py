@@ -235,16 +235,20 @@ class Workload:
         return int(torch.unique(idx).numel())
 
 
-def time_steps(torch, fn, steps, world):
+def time_steps(torch, fn, steps, world, label="timed"):
+    """Run fn(0..steps-1) between two CUDA events on the current stream, bracketed by a
+    barrier and a device synchronise on both sides, inside an NVTX start/end range."""
     barrier(world)
     torch.cuda.synchronize()
     st = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rid = torch.cuda.nvtx.range_start(label)
     e0.record(st)
     for i in range(steps):
         fn(i)
     e1.record(st)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_end(rid)
     barrier(world)
     return e0.elapsed_time(e1) / 1e3
 
@@ -358,8 +362,9 @@ def layer_sweep(torch, hla, inputs, wl, dev, peak):
     return res
 
 
-def traffic_entry(kernel):
-    """DRAM bytes per launch from a committed ncu capture, if the kernel sources are unchanged."""
+def traffic_entry(kernel, units):
+    """DRAM bytes per launch from a committed ncu capture (per streamed unit, times the units
+    of this launch), or None when the kernel sources changed since the counters were taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)[kernel]
@@ -370,14 +375,18 @@ def traffic_entry(kernel):
     for rel in t["sources"]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
-    return t if h.hexdigest() == t["sources_sha256"] else None
+    if h.hexdigest() != t["sources_sha256"]:
+        return None
+    return dict(t, bytes_per_launch=round(t["per_unit_bytes"] * units))
 
 
-def cpu_baseline(wl, n_seq=4):
-    """The fp64 oracle, as it stands, on a bounded sample of the step (host cores)."""
+def cpu_baseline(wl, n_seq=8):
+    """The fp64 oracle, as it stands, on a bounded sample of the step (host cores).  Its
+    inputs are handed over as float32 arrays (exact for bf16 values); the oracle upcasts
+    to float64 itself, as it always does."""
     import oracle
     c = CFG
-    f = lambda t: t.detach().cpu().double().numpy()  # noqa: E731
+    f = lambda t: t.detach().cpu().float().numpy()  # noqa: E731
     p = dict(H=c["H"], dk=c["d"], dv=c["d"], top_k=c["k"], eps=c["eps"],
              gamma_attn=f(wl.w["gamma_attn"]), gamma_moe=f(wl.w["gamma_moe"]),
              W_qkvgb=f(wl.w["W_qkvgb"]), W_o=f(wl.w["W_o"]), W_r=f(wl.w["W_r"]))
@@ -402,7 +411,7 @@ def cpu_baseline(wl, n_seq=4):
         oracle.kda.spec_verify(S_spec, win["q"], win["k"], win["v"], win["alpha"], win["beta"])
         oracle.kda.spec_replay(S_spec, win["q"], win["k"], win["v"], win["alpha"], win["beta"], a)
         return used
-    sample()  # untimed: brings the sampled experts' weights to the host in fp64
+    sample()  # untimed: brings the sampled experts' weights to the host
     t0 = time.perf_counter()
     used = sample()
     dt = time.perf_counter() - t0
@@ -410,8 +419,8 @@ def cpu_baseline(wl, n_seq=4):
     return dict(value=round(nbytes / dt / 1e9, 4), unit="GB/s", cores=len(os.sched_getaffinity(0)),
                 kind="oracle", seconds=round(dt, 2),
                 sample=f"decode layer for {n_seq} of the 64 sequences (one at a time) + speculative "
-                       f"window for 2 of the 16 sequences, fp64 numpy oracle with the sampled "
-                       f"weights already on the host in fp64; bytes credited as for that sample")
+                       f"window for 2 of the 16 sequences, fp64 numpy oracle (inputs as fp32 host "
+                       f"arrays, upcast by the oracle); bytes credited as for that sample")
 
 
 def run_ours(args):
@@ -481,7 +490,7 @@ def run_ours(args):
         ah.copy_(wl.acc, non_blocking=True)
     for i in range(2):
         e2e_step(i)
-    e2e_elapsed = time_steps(torch, e2e_step, args.steps, world)
+    e2e_elapsed = time_steps(torch, e2e_step, args.steps, world, label="e2e")
     e2e_max, _ = reduce_over_ranks(e2e_elapsed, 0, world)
 
     sweeps = {}
@@ -497,7 +506,7 @@ def run_ours(args):
     gu_avg_s = statistics.mean(gu_ms) / 1e3 if gu_ms else None
     gu_b = gateup_bytes(c["M"], U)
     achieved = gu_b / gu_avg_s / 1e9 if gu_avg_s else None
-    tr = traffic_entry("moe_gateup_kernel")
+    tr = traffic_entry("moe_gateup_kernel", U + c["n_shared"])
     out = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -552,6 +561,63 @@ def run_ours(args):
     print(json.dumps(out))
 
 
+# ----------------------------------------------------------------------------- ncu cases
+
+def run_profile(kind, iters=3):
+    """Small cases of the hot kernels for `ncu --set full` captures: a few GB on the
+    device, inputs still larger than L2.  Prints one JSON line describing the case."""
+    import torch
+    from hybrid_linear_attention_gated_gb300 import build, hla, inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    c = CFG
+    g = inputs.generator(500, dev)
+    info = dict(case=kind)
+    if kind == "moe":
+        # 48 experts, 16 tokens, top-8: ~2.6 tokens per active expert (as at batch 64 with
+        # 256 experts) and the same 16-token tile variant as the full workload
+        E, M = 48, 16
+        w = inputs.moe_weights(E, c["Hd"], c["I"], c["n_shared"], g, device=dev)
+        x = inputs.activations(M, c["Hd"], g, dev)
+        idx = torch.empty(M, c["k"], dtype=torch.int32, device=dev)
+        wt = torch.empty(M, c["k"], device=dev)
+        rb = hla.moe_route_topk_workspace_size(M, c["Hd"], E)
+        rws = torch.empty(max(rb, 256), dtype=torch.uint8, device=dev)
+        nb = hla.moe_expert_forward_workspace_size(M, c["Hd"], c["I"], E, c["k"], c["n_shared"])
+        mws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        y = torch.empty(M, c["Hd"], dtype=torch.bfloat16, device=dev)
+        hla.moe_route_topk(M, c["Hd"], E, c["k"], x, w["W_r"], idx, wt, None, rws, rb)
+        U = int(torch.unique(idx).numel())
+        for _ in range(iters):
+            hla.moe_expert_forward(M, c["Hd"], c["I"], E, c["k"], c["n_shared"], x, idx, wt,
+                                   w["W_gate"], w["W_up"], w["W_down"], w["Ws_gate"], w["Ws_up"],
+                                   w["Ws_down"], None, y, mws, nb)
+        info.update(E=E, M=M, active_experts=U, gateup_bytes=gateup_bytes(M, U),
+                    variant=hla.hla_last_variant())
+    elif kind == "kda":
+        B, H, d = 64, c["H"], c["d"]
+        S = torch.randn(B, H, d, d, device=dev).mul_(0.05)
+        u = inputs.kda_inputs((B,), H, d, d, g, dev)
+        o = torch.empty(B, H, d, device=dev)
+        for _ in range(iters):
+            hla.kda_decode_step(B, H, d, d, S, None, u["q"], u["k"], u["v"], u["alpha"], u["beta"], o)
+        info.update(B=B, bytes=kda_bytes(B), variant=hla.hla_last_variant())
+    elif kind == "dense":
+        M, H, d = 64, c["H"], c["d"]
+        W = inputs.weight((4 * H * d + H, c["Hd"]), g, dev)
+        x = inputs.activations(M, c["Hd"], g, dev)
+        outs = [torch.empty(M, H, d, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+        al, be = torch.empty(M, H, d, device=dev), torch.empty(M, H, device=dev)
+        nb = hla.kda_qkvg_proj_workspace_size(M, c["Hd"], H, d, d, 0)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        for _ in range(iters):
+            hla.kda_qkvg_proj(M, c["Hd"], H, d, d, x, W, *outs, al, be, 0, ws, nb)
+        info.update(M=M, weight_bytes=W.numel() * 2, variant=hla.hla_last_variant())
+    torch.cuda.synchronize()
+    print(json.dumps(info))
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -566,7 +632,7 @@ def run_reference(args):
     import oracle
     from hybrid_linear_attention_gated_gb300 import inputs
     c = CFG
-    f = lambda t: t.double().numpy()  # noqa: E731
+    f = lambda t: t.float().numpy()  # noqa: E731  (exact for bf16; the oracle upcasts)
     g = inputs.generator(11)
     lw = inputs.layer_weights(c["Hd"], c["H"], c["d"], c["d"], g)
     W_r = inputs.weight((c["E"], c["Hd"]), g)
@@ -637,7 +703,11 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true")
+    ap.add_argument("--profile", choices=["moe", "kda", "dense"],
+                    help="run one small case of a hot kernel (for ncu captures) and exit")
     args = ap.parse_args()
+    if args.profile:
+        return run_profile(args.profile)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -174,21 +174,28 @@ __global__ void rmsnorm_kernel(int Hd, const uint16_t *__restrict__ x,
     }
 }
 
-// One warp per token: fp32 logits (sum of split partials), top-k on logits (ties to the
-// lower index), sigmoid scores of the chosen experts, renormalised.
-__global__ void router_topk_kernel(const float *__restrict__ part, int split, int M, int E, int k,
-                                   int32_t *topk_idx, float *topk_w, float *logits_out) {
+// One CTA per token: 256 threads sum the split partials of the fp32 logits (each thread a
+// strided subset of experts, slices in increasing order), then one warp picks the top k on
+// the logits (ties to the lower index), takes sigmoid scores of the chosen experts and
+// renormalises them.
+constexpr int kRouterThreads = 256;
+
+__global__ void __launch_bounds__(kRouterThreads)
+    router_topk_kernel(const float *__restrict__ part, int split, int M, int E, int k,
+                       int32_t *topk_idx, float *topk_w, float *logits_out) {
     __shared__ float lg[1024];
     __shared__ float sel[16];
-    const int m = blockIdx.x, lane = threadIdx.x;
+    const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
     const size_t plane = (size_t)M * E;
-    for (int e = lane; e < E; e += 32) {
-        float s = part[(size_t)m * E + e];
-        for (int sl = 1; sl < split; ++sl) s = __fadd_rn(s, part[(size_t)sl * plane + (size_t)m * E + e]);
+    for (int e = tid; e < E; e += kRouterThreads) {
+        const float *src = part + (size_t)m * E + e;
+        float s = src[0];
+        for (int sl = 1; sl < split; ++sl) s = __fadd_rn(s, src[(size_t)sl * plane]);
         lg[e] = s;
         if (logits_out) logits_out[(size_t)m * E + e] = s;
     }
-    __syncwarp();
+    __syncthreads();
+    if (tid >= 32) return;
     for (int j = 0; j < k; ++j) {
         float bv = -INFINITY;
         int be = 0x7fffffff;
@@ -314,7 +321,7 @@ int run_router(int M, int Hd, int E, int k, const hla_bf16 *x, const hla_bf16 *W
     const int split = router_split(M, Hd, E);
     int s = run_dense(M, E, Hd, x, W_r, split, part, nullptr, 0, nullptr, st);
     if (s != HLA_OK) return s;
-    router_topk_kernel<<<M, 32, 0, st>>>(part, split, M, E, k, idx, w, logits);
+    router_topk_kernel<<<M, kRouterThreads, 0, st>>>(part, split, M, E, k, idx, w, logits);
     return launch_status();
 }
 
