@@ -62,6 +62,7 @@ SIGNATURES = {
     "hla_decode_layer": (c_int, [ctypes.POINTER(hla_layer), c_int] + [P] * 4 + [P, c_size_t, P, P]),
     "hla_decode_layer_routing": (c_int, [ctypes.POINTER(hla_layer), c_int, P,
                                          ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p)]),
+    "skinny_proj_splitk_noalloc": (c_int, [c_int] * 3 + [P] * 4 + [c_int, c_int, P]),
     "hla_launch_count": (ctypes.c_ulonglong, []),
     "hla_trace_enable": (c_int, [c_char_p, c_int]),
     "hla_trace_read": (c_int, [ctypes.POINTER(c_float), c_int]),
@@ -244,3 +245,13 @@ def hla_trace_read(max_n=4096):
     if n < 0:
         raise HlaError("hla_trace_read", -n)
     return [buf[i] for i in range(min(n, max_n))]
+
+
+HLA_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def skinny_proj_splitk_noalloc(M, N, K, x, W, residual, y, y_dtype, split, stream=None):
+    """skinny_proj_splitk with its split-K partials in the library's fixed device array
+    (for callers that cannot allocate a workspace); see include/hla.h."""
+    return _check("skinny_proj_splitk_noalloc", load().skinny_proj_splitk_noalloc(
+        M, N, K, _p(x), _p(W), _p(residual), _p(y), y_dtype, split, _stream(stream)))

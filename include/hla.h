@@ -259,6 +259,31 @@ int hla_decode_layer_routing(const hla_layer *L, int M, const void *ws, const in
                              const float **topk_w);
 
 /* ---------------------------------------------------------------------------
+ * skinny_proj_splitk without a workspace.  No counterpart on the source pages: this is
+ * a convenience for callers that cannot allocate device memory when they run a
+ * projection -- for example a server that fixes its whole device-memory budget at
+ * start-up so that no request can later fail for lack of a workspace, a plugin whose
+ * host application owns every allocation, or code on a path where a cudaMalloc would
+ * stall the device.  It computes exactly what skinny_proj_splitk computes, with the same
+ * arguments except the workspace, and allocates nothing: the split-K partials live in
+ * one fixed device array of HLA_NOALLOC_SCRATCH_BYTES (16 MiB) inside the library, which
+ * every GPU that loads the library keeps until the process exits.
+ *  - The split is the one skinny_proj_splitk would use; when its partials
+ *    (split x M x N x 4 bytes) do not fit the array the call returns HLA_ERR_WORKSPACE
+ *    and launches nothing (pass a smaller split, e.g. 1, which needs no scratch).
+ *  - The first call on each device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream capture.
+ *  - All calls share the one array, so calls that can overlap on the GPU (different
+ *    streams, or different host threads) race and give wrong results: serialise them.
+ *    The array keeps the last call's partials; each call overwrites every partial it
+ *    reads, so no clearing is needed.
+ * -------------------------------------------------------------------------*/
+#define HLA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int skinny_proj_splitk_noalloc(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W,
+                               const hla_bf16 *residual, void *y, int y_dtype, int split,
+                               hla_stream stream);
+
+/* ---------------------------------------------------------------------------
  * Instrumentation (off by default; for profiling tools and benchmarks).
  * hla_launch_count: number of kernels this library has launched in the process.
  * hla_trace_enable: time every launch of one kernel family with a CUDA event pair
