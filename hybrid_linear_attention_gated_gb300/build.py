@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libhla.so")
-SOURCES = ["api.cu", "kda.cu", "gemm.cu", "moe.cu", "layer.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "kda.cu", "gemm.cu", "moe.cu", "layer.cu", "noalloc.cu", "tc_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -250,7 +250,18 @@ int launch_dense_nt(const DenseParams &p, cudaStream_t st) {
 
 }  // namespace
 
-int dense_tokens_per_tile(int M) { return M <= 8 ? 8 : 16; }
+bool dense_tc_enabled(int M);
+int dense_tc_split(int M, int N, int K);
+int dense_tc_tile(int M);
+int run_dense_tc(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W, int split, float *part,
+                 void *y, int y_bf16, const hla_bf16 *residual, cudaStream_t st);
+
+// Tokens per tile: 8 or 16 on the mma.sync streaming path, the MMA N (32..256) on the
+// tensor-core path used from 32 tokens up.
+int dense_tokens_per_tile(int M) {
+    if (dense_tc_enabled(M)) return dense_tc_tile(M);
+    return M <= 8 ? 8 : 16;
+}
 
 // Split so that (row blocks x token groups x split) gives about 24 warp items per SM,
 // with at least 4 K steps (128 K values) per item.
@@ -260,6 +271,7 @@ int dense_auto_split(int M, int N, int K) {
     const long ntg = (M + dense_tokens_per_tile(M) - 1) / dense_tokens_per_tile(M);
     const long base = nrb * ntg;
     const long maxs = K / 128 > 0 ? K / 128 : 1;
+    if (!env && dense_tc_enabled(M)) return dense_tc_split(M, N, K);
     long s = env ? atol(env) : (24L * sm_count() + base - 1) / base;
     if (s < 1) s = 1;
     if (s > maxs) s = maxs;
@@ -272,6 +284,8 @@ int router_split(int M, int Hd, int E) { return dense_auto_split(M, E, Hd); }
 // Run x W^T with the streaming tile.  part != nullptr -> fp32 partials [split][M][N].
 int run_dense(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W, int split, float *part,
               void *y, int y_bf16, const hla_bf16 *residual, cudaStream_t st) {
+    if (dense_tc_enabled(M))
+        return run_dense_tc(M, N, K, x, W, split, part, y, y_bf16, residual, st);
     DenseParams p;
     p.W = W; p.x = x; p.M = M; p.N = N; p.K = K; p.split = split;
     const int tt = dense_tokens_per_tile(M);

@@ -1,0 +1,384 @@
+// Tensor-core (tcgen05 + TMA) path of the skinny projections, for 32 or more tokens.
+//
+// At 32-64 tokens every weight byte meets enough tokens that feeding them through the
+// register file (the mma.sync streaming tile) stops keeping up with HBM: "Hyper-optimizing
+// Kimi K3 in vLLM", Part 1 sec. 1, picks kernels per batch size for the projections.  Here
+// a CTA owns 128 weight rows x one K slice:
+//   * one thread issues TMA loads (cp.async.bulk.tensor, 128-byte swizzle) of the 128x64
+//     weight tile and the MTx64 token tile of each K chunk into a ring of shared-memory
+//     stages, completing on per-stage mbarriers;
+//   * one thread issues tcgen05.mma (kind::f16, bf16 in, fp32 accumulate) from the two
+//     shared-memory descriptors into a 128-lane x MT-column accumulator in tensor memory,
+//     and tcgen05.commit releases each stage when its MMAs finish;
+//   * all four warps then read the accumulator back with tcgen05.ld (warp w owns TMEM lanes
+//     32w..32w+31 = weight rows) and store fp32 partials or the final output.
+// Each weight byte is read from HBM once and multiplied against all MT tokens from
+// shared memory.  Every wait is bounded: a wait that gives up records
+// HLA_ERR_DEVICE_TIMEOUT in a device status word and the CTA drains and exits.
+#include <cuda.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace hla {
+
+int dense_tokens_per_tile(int M);
+
+namespace {
+
+constexpr int kTcThreads = 128;
+constexpr int kRows = 128;    // MMA M: weight rows per CTA
+constexpr int kChunk = 64;    // K elements per stage = one 128-byte swizzle atom of bf16
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+__device__ int g_tc_status = 0;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Bounded wait for the phase with the given parity; false (and the status word set) on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    atomicExch(&g_tc_status, HLA_ERR_DEVICE_TIMEOUT);
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major tile written by TMA with 128-byte swizzle;
+// 8-row core-matrix groups 1024 bytes apart (SBO); descriptor version 1; SWIZZLE_128B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;            // leading byte offset (unused with swizzle)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;    // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;            // version
+    d |= static_cast<uint64_t>(2) << 61;            // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
+        " [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct TcParams {
+    int M, N, K;
+    int nrb, split, chunks_per_split, nchunks;
+    float *part;               // [split][M][N] partials, or nullptr
+    void *y;
+    int y_bf16;
+    const uint16_t *residual;
+};
+
+template <int MT>
+__host__ __device__ constexpr int tc_stages() {
+    return (MT * 128 + kRows * 128) * 4 <= 104 * 1024 ? 4 : ((MT * 128 + kRows * 128) * 3 <= 160 * 1024 ? 3 : 2);
+}
+
+template <int MT>
+__host__ __device__ constexpr size_t tc_smem_bytes() {
+    return 1024 + static_cast<size_t>(tc_stages<MT>()) * (kRows * 128 + MT * 128) +
+           (2 * tc_stages<MT>() + 1) * 8 + 16;  // + TMEM address and consumed count
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    dense_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                    const TcParams p) {
+    constexpr int NS = tc_stages<MT>();
+    constexpr uint32_t A_BYTES = kRows * 128, B_BYTES = MT * 128;
+    constexpr uint32_t IDESC = idesc_bf16(kRows, MT);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + NS * A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + NS * B_BYTES);
+    uint64_t *empty = full + NS;
+    uint64_t *done = empty + NS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    int *consumed_slot = reinterpret_cast<int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rb = blockIdx.x % p.nrb, ks = blockIdx.x / p.nrb;
+    const int c0 = ks * p.chunks_per_split;
+    const int c1 = min(p.nchunks, c0 + p.chunks_per_split);
+    const int nmine = c1 > c0 ? c1 - c0 : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(MT)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    int issued = 0, consumed = 0;
+    if (warp == 0 && lane == 0) {
+        // producer: TMA the weight tile and the token tile of each K chunk
+        for (int i = 0; i < nmine; ++i) {
+            const int s = i % NS;
+            if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1)) break;
+            mbar_expect_tx(&full[s], A_BYTES + B_BYTES);
+            const int kx = (c0 + i) * kChunk;
+            tma_load_2d(sA + s * A_BYTES, &tmW, kx, rb * kRows, &full[s]);
+            tma_load_2d(sB + s * B_BYTES, &tmX, kx, 0, &full[s]);
+            issued = i + 1;
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer: 4 x (128 x MT x 16) per stage, accumulating in tensor memory
+        for (int i = 0; i < nmine; ++i) {
+            const int s = i % NS;
+            if (!mbar_wait(&full[s], (i / NS) & 1)) break;
+            tc_fence_after();
+            const uint64_t da = sw128_desc(smem_u32(sA + s * A_BYTES));
+            const uint64_t db = sw128_desc(smem_u32(sB + s * B_BYTES));
+#pragma unroll
+            for (int kk = 0; kk < kChunk / 16; ++kk)
+                umma_bf16(tmem, da + 2 * kk, db + 2 * kk, IDESC, (i > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&empty[s]);
+            consumed = i + 1;
+        }
+        umma_commit(done);  // arrives once every MMA issued above has completed
+        *consumed_slot = consumed;
+    }
+    __syncwarp();
+
+    const bool ok = mbar_wait(done, 0);
+    tc_fence_after();
+    const int row = rb * kRows + warp * 32 + lane;
+    const bool have = ok && nmine > 0;
+#pragma unroll
+    for (int c = 0; c < MT; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+        if (row < p.N) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int m = c + j;
+                if (m >= p.M) break;
+                const float acc = have ? __uint_as_float(v[j]) : 0.f;
+                const size_t o = static_cast<size_t>(m) * p.N + row;
+                if (p.part) {
+                    p.part[static_cast<size_t>(ks) * p.M * p.N + o] = acc;
+                } else {
+                    float val = acc;
+                    if (p.residual) val = __fadd_rn(val, bf16_bits_to_float(p.residual[o]));
+                    if (p.y_bf16)
+                        reinterpret_cast<uint16_t *>(p.y)[o] = float_to_bf16_bits(val);
+                    else
+                        reinterpret_cast<float *>(p.y)[o] = val;
+                }
+            }
+        }
+    }
+    // after a timeout, copies may be in flight that no MMA waited for: wait (bounded) for
+    // those fills before the CTA exits.  At most one unconsumed fill per stage exists, since
+    // the producer never runs more than NS fills ahead of the MMA thread.
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+        for (int i = *consumed_slot; i < issued; ++i) mbar_wait(&full[i % NS], (i / NS) & 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(MT)
+                     : "memory");
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, K] matrix, box = 64 K elements x box_rows rows.
+bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t K, uint32_t box_rows) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {K, rows};
+    const cuuint64_t strides[1] = {K * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunk), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MT>
+int launch_tc(const TcParams &p, const void *W, const void *x, cudaStream_t st) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(dense_tc_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)tc_smem_bytes<MT>()) != cudaSuccess)
+            return HLA_ERR_CUDA;
+        attr_done = true;
+    }
+    CUtensorMap mw, mx;
+    if (!make_map(&mw, W, p.N, p.K, kRows) || !make_map(&mx, x, p.M, p.K, MT)) return HLA_ERR_CUDA;
+    trace_before(kTraceDense, st);
+    dense_tc_kernel<MT><<<p.nrb * p.split, kTcThreads, tc_smem_bytes<MT>(), st>>>(mw, mx, p);
+    trace_after(kTraceDense, st);
+    return launch_status();
+}
+
+}  // namespace
+
+bool dense_tc_enabled(int M) {
+    const char *env = getenv("HLA_DENSE_TC");
+    if (env && env[0] == '0') return false;
+    return M >= 32 && M <= 256;
+}
+
+int dense_tc_tile(int M) { return M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256)); }
+
+// K slices for the tensor-core path, from a small bandwidth model: a CTA keeps about
+// 4 x (16 KB + MT x 128 B) in flight and streams at roughly kCtaBytesPerS; HBM caps the sum;
+// the fp32 partials (split x M x N x 8 bytes written and read back) are extra traffic; a
+// partly filled last wave of CTAs stretches the time.  The smallest split within 2% of the
+// best estimate wins.
+int dense_tc_split(int M, int N, int K) {
+    constexpr double kCtaBytesPerS = 40e9, kHbmBytesPerS = 6.5e12;  // per-CTA rate measured with ncu
+    const int nrb = (N + kRows - 1) / kRows;
+    const int nchunks = (K + kChunk - 1) / kChunk;
+    const int slots = 2 * sm_count();
+    const double wbytes = 2.0 * N * K;
+    int best_s = 1;
+    double best_t = 1e30;
+    const int smax = nchunks / 2 < 64 ? (nchunks / 2 > 1 ? nchunks / 2 : 1) : 64;
+    for (int s = 1; s <= smax; ++s) {
+        const long ctas = (long)nrb * s;
+        const double conc = ctas < slots ? (double)ctas : (double)slots;
+        double bw = conc * kCtaBytesPerS;
+        if (bw > kHbmBytesPerS) bw = kHbmBytesPerS;
+        const double waves = (double)((ctas + slots - 1) / slots);
+        const double q = ctas > slots ? waves * slots / (double)ctas : 1.0;
+        const double t = (wbytes + (s > 1 ? 8.0 * s * M * N : 0.0)) / bw * q;
+        if (t < best_t * 0.98) {
+            best_t = t;
+            best_s = s;
+        }
+    }
+    return best_s;
+}
+
+int run_dense_tc(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W, int split, float *part,
+                 void *y, int y_bf16, const hla_bf16 *residual, cudaStream_t st) {
+    TcParams p;
+    p.M = M; p.N = N; p.K = K;
+    p.nrb = (N + kRows - 1) / kRows;
+    p.nchunks = (K + kChunk - 1) / kChunk;
+    p.split = split;
+    p.chunks_per_split = (p.nchunks + split - 1) / split;
+    p.part = part; p.y = y; p.y_bf16 = y_bf16; p.residual = residual;
+    switch (dense_tc_tile(M)) {
+        case 32: return launch_tc<32>(p, W, x, st);
+        case 64: return launch_tc<64>(p, W, x, st);
+        case 128: return launch_tc<128>(p, W, x, st);
+        default: return launch_tc<256>(p, W, x, st);
+    }
+}
+
+}  // namespace hla
+
+// Reads and clears the status word the tensor-core kernels set when a bounded wait gives up.
+extern "C" int hla_device_status(void) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, hla::g_tc_status, sizeof(int)) != cudaSuccess) return HLA_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(hla::g_tc_status, &zero, sizeof(int)) != cudaSuccess) return HLA_ERR_CUDA;
+    }
+    return v;
+}

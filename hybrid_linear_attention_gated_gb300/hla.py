@@ -64,6 +64,7 @@ SIGNATURES = {
                                          ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p)]),
     "skinny_proj_splitk_noalloc": (c_int, [c_int] * 3 + [P] * 4 + [c_int, c_int, P]),
     "hla_launch_count": (ctypes.c_ulonglong, []),
+    "hla_device_status": (c_int, []),
     "hla_trace_enable": (c_int, [c_char_p, c_int]),
     "hla_trace_read": (c_int, [ctypes.POINTER(c_float), c_int]),
 }
@@ -255,3 +256,7 @@ def skinny_proj_splitk_noalloc(M, N, K, x, W, residual, y, y_dtype, split, strea
     (for callers that cannot allocate a workspace); see include/hla.h."""
     return _check("skinny_proj_splitk_noalloc", load().skinny_proj_splitk_noalloc(
         M, N, K, _p(x), _p(W), _p(residual), _p(y), y_dtype, split, _stream(stream)))
+
+
+def hla_device_status():
+    return load().hla_device_status()

@@ -295,6 +295,10 @@ int skinny_proj_splitk_noalloc(int M, int N, int K, const hla_bf16 *x, const hla
  * Not thread-safe; meant for one benchmarking thread.
  * -------------------------------------------------------------------------*/
 unsigned long long hla_launch_count(void);
+/* Reads and clears the device status word: 0, or HLA_ERR_DEVICE_TIMEOUT when a bounded
+ * device-side wait (the tensor-core projection's pipeline barriers) gave up since the last
+ * read.  Synchronous (copies 4 bytes from the device); HLA_ERR_CUDA if that copy fails. */
+int hla_device_status(void);
 int hla_trace_enable(const char *kernel, int capacity);
 int hla_trace_read(float *ms_out, int max_n);
 

@@ -78,6 +78,53 @@ def test_split_counts_agree(dev):
         assert frob_rel(f64(y), f64(outs[0])) < 1e-5
 
 
+@pytest.mark.parametrize("M,N,K", [(32, 1000, 4000), (33, 16416, 512), (64, 7168, 4096),
+                                   (100, 300, 2048), (128, 128, 64), (200, 1030, 1024),
+                                   (256, 256, 7168)])
+def test_tensor_core_projection(dev, M, N, K, monkeypatch):
+    """tcgen05 + TMA path (32..256 tokens): ragged rows, K not a multiple of the 64-wide TMA
+    box (zero-filled tail), every tile width; against the oracle and the mma.sync path."""
+    g = inputs.generator(M * 3 + N + K)
+    x = inputs.activations(M, K, g).to(dev)
+    W = inputs.weight((N, K), g).to(dev)
+    y = torch.empty(M, N, device=dev)
+    ws = _ws(hla.skinny_proj_splitk_workspace_size(M, N, K, 0), dev)
+    assert hla.hla_device_status() == 0
+    hla.skinny_proj_splitk(M, N, K, x, W, None, y, hla.HLA_F32, 0, ws, ws.numel())
+    variant = hla.hla_last_variant()
+    torch.cuda.synchronize()
+    assert hla.hla_device_status() == 0
+    tt = int(variant.split("tt")[1].split(",")[0])
+    assert tt >= 32 and tt >= M, variant
+    ref = oracle.moe.linear(f64(x), f64(W))
+    assert frob_rel(f64(y), ref) < PROJ_FROB_REL_F32
+    monkeypatch.setenv("HLA_DENSE_TC", "0")
+    y2 = torch.empty(M, N, device=dev)
+    ws2 = _ws(hla.skinny_proj_splitk_workspace_size(M, N, K, 0), dev)
+    hla.skinny_proj_splitk(M, N, K, x, W, None, y2, hla.HLA_F32, 0, ws2, ws2.numel())
+    assert "tt16" in hla.hla_last_variant()
+    torch.cuda.synchronize()
+    assert frob_rel(f64(y), f64(y2)) < 1e-5
+
+
+def test_tensor_core_split_counts_agree(dev):
+    M, N, K = 64, 640, 2048
+    g = inputs.generator(4)
+    x, W = inputs.activations(M, K, g).to(dev), inputs.weight((N, K), g).to(dev)
+    r = inputs.activations(M, N, g).to(dev)
+    outs = []
+    for split in (1, 2, 3, 8, 32):
+        y = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+        ws = _ws(hla.skinny_proj_splitk_workspace_size(M, N, K, split), dev)
+        hla.skinny_proj_splitk(M, N, K, x, W, r, y, hla.HLA_BF16, split, ws, ws.numel())
+        outs.append(y)
+    torch.cuda.synchronize()
+    ref = oracle.moe.linear(f64(x), f64(W)) + f64(r)
+    for y in outs:
+        assert frob_rel(f64(y), ref) < PROJ_FROB_REL_BF16
+    assert hla.hla_device_status() == 0
+
+
 @pytest.mark.parametrize("M,Hd,H,d", [(1, 256, 4, 64), (5, 512, 2, 128), (64, 1024, 4, 128)])
 def test_qkvg_projection(dev, M, Hd, H, d):
     g = inputs.generator(M + Hd)
