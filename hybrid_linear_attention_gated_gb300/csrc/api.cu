@@ -1,6 +1,7 @@
 // Status strings, variant reporting and small device queries for the C ABI.
 #include <atomic>
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <vector>
@@ -40,6 +41,11 @@ void trace_after(int kernel, cudaStream_t st) {
     if (kernel == 0 || kernel != g_trace.kernel || g_trace.count >= g_trace.capacity) return;
     cudaEventRecord(g_trace.stop[g_trace.count], st);
     ++g_trace.count;
+}
+
+int prefetch_mask() {
+    const char *env = getenv("HLA_PREFETCH_MASK");
+    return env ? (atoi(env) & 7) : -1;
 }
 
 int sm_count() {

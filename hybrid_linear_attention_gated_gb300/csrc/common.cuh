@@ -37,6 +37,13 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Which side-stream L2 prefetches run when a prefetch stream is given: a bit mask from the
+// tuning override HLA_PREFETCH_MASK, or -1 for the measured default policy.
+// kPrefetchLayer: output-projection + router weights during the KDA step;
+// kPrefetchSharedGateUp / kPrefetchSharedDown: the shared experts' weights during dispatch.
+enum { kPrefetchLayer = 1, kPrefetchSharedGateUp = 2, kPrefetchSharedDown = 4 };
+int prefetch_mask();
+
 #define HLA_REQUIRE(cond, status) \
     do {                          \
         if (!(cond)) return (status); \

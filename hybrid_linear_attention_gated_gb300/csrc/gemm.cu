@@ -33,19 +33,24 @@ struct DenseParams {
     const uint16_t *residual;  // direct epilogue residual [M][N] or nullptr
 };
 
+// Warp item: 32 weight rows (two 16-row MMA tiles that share the token fragments) x one K
+// slice x one group of 8*NT tokens.
 template <int NT, int UNROLL>
 __global__ void __launch_bounds__(kDenseThreads) dense_stream_kernel(const DenseParams p) {
     const int item = (blockIdx.x * kDenseThreads + threadIdx.x) >> 5;
-    const int nrb = (p.N + 15) >> 4;
+    const int nrb = (p.N + 31) >> 5;
     if (item >= nrb * p.split * p.ntg) return;  // whole warp leaves together
     const int tg = item % p.ntg;
     const int rest = item / p.ntg;
     const int ks = rest % p.split;
     const int rb = rest / p.split;
     const int g = (threadIdx.x & 31) >> 2;
+    const int rbase = rb * 32;
 
-    const uint16_t *wg[1] = {p.W + (size_t)min(rb * 16 + g, p.N - 1) * p.K};
-    const uint16_t *wg8[1] = {p.W + (size_t)min(rb * 16 + g + 8, p.N - 1) * p.K};
+    const uint16_t *wg[2] = {p.W + (size_t)min(rbase + g, p.N - 1) * p.K,
+                             p.W + (size_t)min(rbase + 16 + g, p.N - 1) * p.K};
+    const uint16_t *wg8[2] = {p.W + (size_t)min(rbase + g + 8, p.N - 1) * p.K,
+                              p.W + (size_t)min(rbase + 16 + g + 8, p.N - 1) * p.K};
     const uint16_t *xr[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -53,30 +58,35 @@ __global__ void __launch_bounds__(kDenseThreads) dense_stream_kernel(const Dense
     int kb, ke;
     k_slice(p.K, p.split, ks, kb, ke);
 
-    float acc[1][NT][4];
+    float acc[2][NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[0][nt][e] = 0.f;
-    warp_stream_tile<1, NT, UNROLL>(wg, wg8, xr, kb, ke, acc);
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[h][nt][e] = 0.f;
+    warp_stream_tile<2, NT, UNROLL>(wg, wg8, xr, kb, ke, acc);
 
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
+    for (int h = 0; h < 2; ++h) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int r = rb * 16 + acc_row(e);
-            const int m = tg * 8 * NT + acc_tok(nt, e);
-            if (r >= p.N || m >= p.M) continue;
-            const size_t o = (size_t)m * p.N + r;
-            if (p.part) {
-                p.part[(size_t)ks * p.M * p.N + o] = acc[0][nt][e];
-            } else {
-                float v = acc[0][nt][e];
-                if (p.residual) v = __fadd_rn(v, bf16_bits_to_float(p.residual[o]));
-                if (p.y_bf16)
-                    reinterpret_cast<uint16_t *>(p.y)[o] = float_to_bf16_bits(v);
-                else
-                    reinterpret_cast<float *>(p.y)[o] = v;
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = rbase + 16 * h + acc_row(e);
+                const int m = tg * 8 * NT + acc_tok(nt, e);
+                if (r >= p.N || m >= p.M) continue;
+                const size_t o = (size_t)m * p.N + r;
+                if (p.part) {
+                    p.part[(size_t)ks * p.M * p.N + o] = acc[h][nt][e];
+                } else {
+                    float v = acc[h][nt][e];
+                    if (p.residual) v = __fadd_rn(v, bf16_bits_to_float(p.residual[o]));
+                    if (p.y_bf16)
+                        reinterpret_cast<uint16_t *>(p.y)[o] = float_to_bf16_bits(v);
+                    else
+                        reinterpret_cast<float *>(p.y)[o] = v;
+                }
             }
         }
     }
@@ -240,7 +250,7 @@ __global__ void l2_prefetch_kernel(const char *p, size_t bytes, uint32_t chunk) 
 
 template <int NT>
 int launch_dense_nt(const DenseParams &p, cudaStream_t st) {
-    const long items = (long)((p.N + 15) / 16) * p.split * p.ntg;
+    const long items = (long)((p.N + 31) / 32) * p.split * p.ntg;
     const long blocks = (items * 32 + kDenseThreads - 1) / kDenseThreads;
     trace_before(kTraceDense, st);
     dense_stream_kernel<NT, 4><<<(unsigned)blocks, kDenseThreads, 0, st>>>(p);
@@ -263,11 +273,11 @@ int dense_tokens_per_tile(int M) {
     return M <= 8 ? 8 : 16;
 }
 
-// Split so that (row blocks x token groups x split) gives about 24 warp items per SM,
+// Split so that (32-row blocks x token groups x split) gives about 24 warp items per SM,
 // with at least 4 K steps (128 K values) per item.
 int dense_auto_split(int M, int N, int K) {
     const char *env = getenv("HLA_DENSE_SPLIT");
-    const long nrb = (N + 15) / 16;
+    const long nrb = (N + 31) / 32;
     const long ntg = (M + dense_tokens_per_tile(M) - 1) / dense_tokens_per_tile(M);
     const long base = nrb * ntg;
     const long maxs = K / 128 > 0 ? K / 128 : 1;

@@ -4,10 +4,11 @@
 //     -> RMSNorm -> router -> routed + shared experts + residual -> y
 // ("Hyper-optimizing Kimi K3 in vLLM", Part 1 secs. 1-4; "Kimi K3: From Day-0
 // Availability to Optimized Inference": residual adds and normalisation around the
-// projections).  With a prefetch stream, the output-projection and router weights are
-// pulled into L2 while the latency-bound KDA step runs, and the MoE call warms the
-// shared expert while routing bookkeeping runs (Part 1 sec. 4).  All scratch lives in
-// the caller's workspace; nothing here allocates or synchronises.
+// projections).  The prefetch stream is passed to the MoE call, which warms the shared
+// expert's rows in L2 during dispatch when several token groups will read them (Part 1
+// sec. 4); warming the output-projection and router weights during the KDA step is
+// available through HLA_PREFETCH_MASK.  All scratch lives in the caller's workspace;
+// nothing here allocates or synchronises.
 #include "common.cuh"
 
 namespace hla {
@@ -92,7 +93,11 @@ extern "C" int hla_decode_layer(const hla_layer *L, int M, const hla_bf16 *x, fl
                            f32(lo.alpha), f32(lo.beta), 0, w + lo.qkvg_ws, lo.qkvg_bytes,
                            stream)) != HLA_OK)
         return r;
-    if (pf) {
+    // W_o / W_r warming during the KDA step is off unless asked for: it measured neutral at
+    // batch 64 and slower at batch 1-8 (the stream flushes L2 before the o-projection).
+    const int pm = prefetch_mask();
+    const bool layer_pf = pf && pm >= 0 && (pm & kPrefetchLayer);
+    if (layer_pf) {
         if (!g_fork && cudaEventCreateWithFlags(&g_fork, cudaEventDisableTiming) != cudaSuccess)
             return HLA_ERR_CUDA;
         if (!g_join && cudaEventCreateWithFlags(&g_join, cudaEventDisableTiming) != cudaSuccess)
@@ -121,7 +126,7 @@ extern "C" int hla_decode_layer(const hla_layer *L, int M, const hla_bf16 *x, fl
                                 L->W_up, L->W_down, L->Ws_gate, L->Ws_up, L->Ws_down, bf(lo.r), y,
                                 w + lo.moe_ws, lo.moe_bytes, stream, prefetch_stream)) != HLA_OK)
         return r;
-    if (pf && cudaStreamWaitEvent(st, g_join, 0) != cudaSuccess) return HLA_ERR_CUDA;
+    if (layer_pf && cudaStreamWaitEvent(st, g_join, 0) != cudaSuccess) return HLA_ERR_CUDA;
     set_variant("decode_layer%s", pf ? "<prefetch>" : "");
     return HLA_OK;
 }

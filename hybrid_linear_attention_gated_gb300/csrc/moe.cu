@@ -7,7 +7,8 @@
 // use the memory bandwidth.
 //
 // Pipeline (all on device, no host round trip; sizes the host does not know -- the
-// number of active experts -- are read by persistent kernels from the workspace):
+// number of active experts -- are read by persistent kernels from the workspace, whose
+// warps claim work items from a counter):
 //   1. dispatch   : one CTA groups the M*k (token, slot) pairs by expert (counting
 //                   sort, stable by pair index), lists the active experts (shared
 //                   experts first) and prefix-sums their work items.
@@ -15,8 +16,9 @@
 //                   K slice for up to 16 of expert e's tokens; SiLU(g)*u -> h (bf16),
 //                   or fp32 partials when K is split (small M, to fill the GPU).
 //   3. [reduce]   : h = SiLU(sum g) * (sum u) over the K slices, fixed order.
-//   4. down       : persistent warps stream 16 rows of W_down[e] for the tokens'
-//                   h rows -> one fp32 row per (token, slot).
+//   4. down       : persistent warps stream 32 rows of W_down[e] (two 16-row MMA tiles
+//                   sharing the token fragments) for the tokens' h rows -> one fp32 row per
+//                   (token, slot).
 //   5. combine    : y[m] = sum_j w[m,j] * y[m,j] + sum_s y[m,k+s] (+ residual), fixed order.
 // Each active expert's weights are read from HBM once per call; when an expert has
 // more than 16 tokens, its token groups are adjacent work items that stream the same
@@ -29,6 +31,9 @@
 namespace hla {
 
 int run_l2_prefetch(const void *ptr, size_t bytes, cudaStream_t st);
+int dense_tc_split(int M, int N, int K);
+int run_dense_tc(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W, int split, float *part,
+                 void *y, int y_bf16, const hla_bf16 *residual, cudaStream_t st);
 
 namespace {
 
@@ -37,12 +42,15 @@ constexpr int kDispatchThreads = 1024;
 
 struct MoeLayout {
     int M, Hd, I, E, k, nsh, P, U_max, KS, TT;
+    bool shared_tc;      // shared experts on the tensor-core path instead of grouped work units
+    int s_gu, s_dn;      // K slices of the shared experts' tensor-core products
     size_t off_meta, off_unit_expert, off_unit_off, off_item_gu, off_item_dn, off_pos_token,
-        off_pos_slot, off_h, off_part_g, off_part_u, off_ypart, total;
+        off_pos_slot, off_h, off_part_g, off_part_u, off_ypart, off_sh_g, off_sh_u, off_sh_d, total;
 };
 
 struct MoeArgs {
     int M, Hd, I, E, k, nsh, P, KS, TT;
+    int nsh_units;  // shared experts run as grouped work units (0 when on the tensor-core path)
     const uint16_t *x;
     const int32_t *topk_idx;
     const float *topk_w;
@@ -78,6 +86,14 @@ MoeLayout moe_layout(int M, int Hd, int I, int E, int k, int nsh) {
     L.U_max = E + nsh;
     L.KS = moe_gateup_split(M, I, E, k, nsh);
     L.TT = moe_tokens_per_tile(M);
+    // Optional (HLA_SHARED_TC=1): past 16 tokens run each shared expert as a dense SwiGLU
+    // over all M tokens on the tensor-core path instead of as a grouped work unit.  Off by
+    // default: in the decode layer at batch 64 the grouped unit with its gate/up weights
+    // warmed in L2 measured 3146 us per layer against 3515 us for this path.
+    const char *env = getenv("HLA_SHARED_TC");
+    L.shared_tc = nsh > 0 && M > 16 && env && env[0] == '1';
+    L.s_gu = L.shared_tc ? dense_tc_split(M, I, Hd) : 0;
+    L.s_dn = L.shared_tc ? dense_tc_split(M, Hd, I) : 0;
     size_t o = 0;
     auto take = [&](size_t bytes) {
         const size_t at = o;
@@ -95,6 +111,9 @@ MoeLayout moe_layout(int M, int Hd, int I, int E, int k, int nsh) {
     L.off_part_g = take(L.KS > 1 ? (size_t)L.KS * L.P * I * sizeof(float) : 0);
     L.off_part_u = take(L.KS > 1 ? (size_t)L.KS * L.P * I * sizeof(float) : 0);
     L.off_ypart = take((size_t)L.P * Hd * sizeof(float));
+    L.off_sh_g = take(L.shared_tc ? (size_t)L.s_gu * M * I * sizeof(float) : 0);
+    L.off_sh_u = take(L.shared_tc ? (size_t)L.s_gu * M * I * sizeof(float) : 0);
+    L.off_sh_d = take(L.shared_tc ? (size_t)L.s_dn * M * Hd * sizeof(float) : 0);
     L.total = o;
     return L;
 }
@@ -132,7 +151,7 @@ __global__ void __launch_bounds__(kDispatchThreads) moe_dispatch_kernel(const Mo
     __shared__ int warp_tot[33];
     const int tid = threadIdx.x;
     const int npairs = a.M * a.k;
-    const int nrb_gu = (a.I + 15) / 16, nrb_dn = (a.Hd + 15) / 16;
+    const int nrb_gu = (a.I + 15) / 16, nrb_dn = (a.Hd + 31) / 32;
 
     cnt[tid] = 0;
     run[tid] = 0;
@@ -173,19 +192,21 @@ __global__ void __launch_bounds__(kDispatchThreads) moe_dispatch_kernel(const Mo
         a.pos_token[i] = m;
         a.pos_slot[i] = m * (a.k + a.nsh) + a.k + s;
     }
-    // unit tables: shared experts are units 0..nsh-1, routed experts follow by id
-    if (tid < a.nsh) {
+    // unit tables: shared experts (when grouped) are units 0..nsh-1, routed experts follow by id
+    if (tid < a.nsh_units) {
         a.unit_expert[tid] = a.E + tid;
         a.unit_off[tid] = tid * a.M;
     }
     if (tid < a.E && c > 0) {
-        a.unit_expert[a.nsh + uid[tid]] = tid;
-        a.unit_off[a.nsh + uid[tid]] = routed0 + base[tid];
+        a.unit_expert[a.nsh_units + uid[tid]] = tid;
+        a.unit_off[a.nsh_units + uid[tid]] = routed0 + base[tid];
     }
-    const int U = a.nsh + nact;
+    const int U = a.nsh_units + nact;
     if (tid == 0) {
         a.unit_off[U] = routed0 + nvalid;
         a.meta[0] = U;
+        a.meta[3] = 0;  // next gate/up work item to hand out
+        a.meta[4] = 0;  // next down work item to hand out
     }
     __syncthreads();
     int ig = 0, id = 0;
@@ -210,6 +231,15 @@ __global__ void __launch_bounds__(kDispatchThreads) moe_dispatch_kernel(const Mo
     }
 }
 
+// Work items are handed out dynamically: lane 0 of a warp claims the next index from a
+// counter the dispatch kernel reset, so warps that start late or run slow simply take fewer
+// items (the result of an item does not depend on which warp computes it).
+__device__ __forceinline__ int claim_item(int *counter) {
+    int it = 0;
+    if ((threadIdx.x & 31) == 0) it = atomicAdd(counter, 1);
+    return __shfl_sync(0xffffffffu, it, 0);
+}
+
 // largest u in [0, U) with pref[u] <= it
 __device__ __forceinline__ int find_unit(const int *pref, int U, int it) {
     int lo = 0, hi = U - 1;
@@ -224,10 +254,8 @@ template <int NT>
 __global__ void __launch_bounds__(kMoeThreads) moe_gateup_kernel(const MoeArgs a) {
     const int U = a.meta[0];
     const int total = a.item_gu[U];
-    const int nwarps = gridDim.x * (kMoeThreads / 32);
     const int g = (threadIdx.x & 31) >> 2;
-    const int nrb = (a.I + 15) / 16;
-    for (int it = blockIdx.x * (kMoeThreads / 32) + (threadIdx.x >> 5); it < total; it += nwarps) {
+    for (int it = claim_item(&a.meta[3]); it < total; it = claim_item(&a.meta[3])) {
         const int u = find_unit(a.item_gu, U, it);
         const int local = it - a.item_gu[u];
         const int p0 = a.unit_off[u], p1 = a.unit_off[u + 1];
@@ -236,7 +264,6 @@ __global__ void __launch_bounds__(kMoeThreads) moe_gateup_kernel(const MoeArgs a
         const int rest = local / ntg;
         const int ks = rest % a.KS;
         const int rb = rest / a.KS;
-        (void)nrb;
         const int e = a.unit_expert[u];
         const size_t eoff = (size_t)(e < a.E ? e : e - a.E) * a.I * a.Hd;
         const uint16_t *Wg = (e < a.E ? a.W_gate : a.Ws_gate) + eoff;
@@ -284,8 +311,10 @@ __global__ void __launch_bounds__(kMoeThreads) moe_gateup_kernel(const MoeArgs a
 __global__ void moe_swiglu_reduce_kernel(const MoeArgs a) {
     const int n = a.meta[0];
     const int used = a.unit_off[n];  // positions in use
+    // positions of shared experts on the tensor-core path are not grouped units: skip them
+    const size_t first = (size_t)(a.nsh - a.nsh_units) * a.M * a.I;
     const size_t total = (size_t)used * a.I, plane = (size_t)a.P * a.I;
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+    for (size_t i = first + blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
         float g = a.part_g[i], u = a.part_u[i];
         for (int s = 1; s < a.KS; ++s) {
@@ -300,21 +329,22 @@ template <int NT>
 __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(const MoeArgs a) {
     const int U = a.meta[0];
     const int total = a.item_dn[U];
-    const int nwarps = gridDim.x * (kMoeThreads / 32);
     const int g = (threadIdx.x & 31) >> 2;
-    for (int it = blockIdx.x * (kMoeThreads / 32) + (threadIdx.x >> 5); it < total; it += nwarps) {
+    for (int it = claim_item(&a.meta[4]); it < total; it = claim_item(&a.meta[4])) {
         const int u = find_unit(a.item_dn, U, it);
         const int local = it - a.item_dn[u];
         const int p0 = a.unit_off[u], p1 = a.unit_off[u + 1];
         const int ntg = (p1 - p0 + a.TT - 1) / a.TT;
         const int tg = local % ntg;
-        const int rb = local / ntg;
+        const int rb = local / ntg;  // a block of 32 rows: two 16-row MMA tiles share the tokens
         const int e = a.unit_expert[u];
         const uint16_t *Wd = (e < a.E ? a.W_down : a.Ws_down) +
                              (size_t)(e < a.E ? e : e - a.E) * a.Hd * a.I;
-        const int r0 = min(rb * 16 + g, a.Hd - 1), r1 = min(rb * 16 + g + 8, a.Hd - 1);
-        const uint16_t *wg[1] = {Wd + (size_t)r0 * a.I};
-        const uint16_t *wg8[1] = {Wd + (size_t)r1 * a.I};
+        const int rbase = rb * 32;
+        const uint16_t *wg[2] = {Wd + (size_t)min(rbase + g, a.Hd - 1) * a.I,
+                                 Wd + (size_t)min(rbase + 16 + g, a.Hd - 1) * a.I};
+        const uint16_t *wg8[2] = {Wd + (size_t)min(rbase + g + 8, a.Hd - 1) * a.I,
+                                  Wd + (size_t)min(rbase + 16 + g + 8, a.Hd - 1) * a.I};
         const int pt = p0 + tg * a.TT;
         const uint16_t *xr[NT];
 #pragma unroll
@@ -322,20 +352,25 @@ __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(const MoeArgs a) 
             const int p = pt + nt * 8 + g;
             xr[nt] = a.h + (size_t)(p < p1 ? p : pt) * a.I;
         }
-        float acc[1][NT][4];
+        float acc[2][NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[0][nt][q] = 0.f;
-        warp_stream_tile<1, NT, 4>(wg, wg8, xr, 0, a.I, acc);
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+                for (int q = 0; q < 4; ++q) acc[h][nt][q] = 0.f;
+        warp_stream_tile<2, NT, 4>(wg, wg8, xr, 0, a.I, acc);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int row = rb * 16 + acc_row(q);
-                const int p = pt + acc_tok(nt, q);
-                if (row >= a.Hd || p >= p1) continue;
-                a.ypart[(size_t)a.pos_slot[p] * a.Hd + row] = acc[0][nt][q];
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int row = rbase + 16 * h + acc_row(q);
+                    const int p = pt + acc_tok(nt, q);
+                    if (row >= a.Hd || p >= p1) continue;
+                    a.ypart[(size_t)a.pos_slot[p] * a.Hd + row] = acc[h][nt][q];
+                }
             }
         }
     }
@@ -372,6 +407,35 @@ __global__ void moe_combine_kernel(const MoeArgs a) {
         make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
 }
 
+// Shared expert on the tensor-core path: h = SiLU(sum of gate slices) * (sum of up slices),
+// written into the shared expert's h rows (positions s*M .. s*M+M-1).
+__global__ void shared_swiglu_kernel(const float *__restrict__ pg, const float *__restrict__ pu,
+                                     int split, int M, int I, uint16_t *h) {
+    const size_t total = (size_t)M * I;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        float g = pg[i], u = pu[i];
+        for (int s = 1; s < split; ++s) {
+            g = __fadd_rn(g, pg[s * total + i]);
+            u = __fadd_rn(u, pu[s * total + i]);
+        }
+        h[i] = float_to_bf16_bits(__fmul_rn(silu_f(g), u));
+    }
+}
+
+// Sum of the down-projection slices into the (token, slot) rows of the expert outputs.
+__global__ void shared_down_reduce_kernel(const float *__restrict__ pd, int split, int M, int Hd,
+                                          int S, int slot, float *ypart) {
+    const size_t total = (size_t)M * Hd;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        float d = pd[i];
+        for (int s = 1; s < split; ++s) d = __fadd_rn(d, pd[s * total + i]);
+        const size_t m = i / Hd, n = i % Hd;
+        ypart[(m * S + slot) * Hd + n] = d;
+    }
+}
+
 template <typename K>
 int persistent_grid(K kernel) {
     int per_sm = 0;
@@ -406,6 +470,7 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     char *w = reinterpret_cast<char *>(ws);
     MoeArgs a;
     a.M = M; a.Hd = Hd; a.I = I; a.E = E; a.k = k; a.nsh = nsh; a.P = L.P; a.KS = L.KS; a.TT = L.TT;
+    a.nsh_units = L.shared_tc ? 0 : nsh;
     a.x = x; a.topk_idx = topk_idx; a.topk_w = topk_w;
     a.W_gate = W_gate; a.W_up = W_up; a.W_down = W_down;
     a.Ws_gate = Ws_gate; a.Ws_up = Ws_up; a.Ws_down = Ws_down;
@@ -422,21 +487,49 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     a.part_u = reinterpret_cast<float *>(w + L.off_part_u);
     a.ypart = reinterpret_cast<float *>(w + L.off_ypart);
 
-    const bool side = pf != nullptr && nsh > 0;
+    // Default: warm the shared experts' gate/up rows in L2 while dispatch runs, but only when
+    // several token groups will stream those rows at the same time (more than one tile of
+    // tokens); with a single token group any prefetch only competes with the weight stream
+    // (measured +11% per layer at batch 1, +19% at batch 8).
+    const int pm = prefetch_mask();
+    const int mask = pm >= 0 ? pm & (kPrefetchSharedGateUp | kPrefetchSharedDown)
+                             : ((!L.shared_tc && M > L.TT) ? kPrefetchSharedGateUp : 0);
+    const bool side = pf != nullptr && nsh > 0 && mask != 0;
     if (side) {
         if (!g_moe_events.ok()) return HLA_ERR_CUDA;
         if (cudaEventRecord(g_moe_events.fork, st) != cudaSuccess) return HLA_ERR_CUDA;
         if (cudaStreamWaitEvent(pf, g_moe_events.fork, 0) != cudaSuccess) return HLA_ERR_CUDA;
         const size_t mat = (size_t)nsh * I * Hd * sizeof(uint16_t);
-        int r = run_l2_prefetch(Ws_gate, mat, pf);
-        if (r == HLA_OK) r = run_l2_prefetch(Ws_up, mat, pf);
-        if (r == HLA_OK) r = run_l2_prefetch(Ws_down, mat, pf);
+        int r = HLA_OK;
+        if (mask & kPrefetchSharedGateUp) {
+            r = run_l2_prefetch(Ws_gate, mat, pf);
+            if (r == HLA_OK) r = run_l2_prefetch(Ws_up, mat, pf);
+        }
+        if (r == HLA_OK && (mask & kPrefetchSharedDown)) r = run_l2_prefetch(Ws_down, mat, pf);
         if (r != HLA_OK) return r;
         if (cudaEventRecord(g_moe_events.join, pf) != cudaSuccess) return HLA_ERR_CUDA;
     }
 
+    int r;
+    if (L.shared_tc) {
+        float *pg = reinterpret_cast<float *>(w + L.off_sh_g);
+        float *pu = reinterpret_cast<float *>(w + L.off_sh_u);
+        float *pd = reinterpret_cast<float *>(w + L.off_sh_d);
+        const int grid = 2 * sm_count();
+        for (int s = 0; s < nsh; ++s) {
+            const size_t eo = (size_t)s * I * Hd;
+            hla_bf16 *hs = a.h + (size_t)s * M * I;
+            if ((r = run_dense_tc(M, I, Hd, x, Ws_gate + eo, L.s_gu, pg, nullptr, 0, nullptr, st)) != HLA_OK) return r;
+            if ((r = run_dense_tc(M, I, Hd, x, Ws_up + eo, L.s_gu, pu, nullptr, 0, nullptr, st)) != HLA_OK) return r;
+            shared_swiglu_kernel<<<grid, 256, 0, st>>>(pg, pu, L.s_gu, M, I, hs);
+            if ((r = launch_status()) != HLA_OK) return r;
+            if ((r = run_dense_tc(M, Hd, I, hs, Ws_down + eo, L.s_dn, pd, nullptr, 0, nullptr, st)) != HLA_OK) return r;
+            shared_down_reduce_kernel<<<grid, 256, 0, st>>>(pd, L.s_dn, M, Hd, k + nsh, k + s, a.ypart);
+            if ((r = launch_status()) != HLA_OK) return r;
+        }
+    }
     moe_dispatch_kernel<<<1, kDispatchThreads, 0, st>>>(a);
-    int r = launch_status();
+    r = launch_status();
     if (r != HLA_OK) return r;
     trace_before(kTraceMoeGateup, st);
     if (L.TT == 8) {
@@ -470,7 +563,7 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     moe_combine_kernel<<<cgrid, 128, 0, st>>>(a);
     if ((r = launch_status()) != HLA_OK) return r;
     if (side && cudaStreamWaitEvent(st, g_moe_events.join, 0) != cudaSuccess) return HLA_ERR_CUDA;
-    set_variant("moe<tt%d,ks%d%s>", L.TT, L.KS, side ? ",prefetch" : "");
+    set_variant("moe<tt%d,ks%d%s%s>", L.TT, L.KS, L.shared_tc ? ",shared_tc" : "", side ? ",prefetch" : "");
     return HLA_OK;
 }
 

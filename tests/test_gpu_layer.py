@@ -67,26 +67,29 @@ def test_decode_layer(dev, full_moe, layer, M):
     assert checked >= 1
 
 
-def test_layer_prefetch_is_bitwise_neutral(dev, layer):
+@pytest.mark.parametrize("M,mask", [(8, "7"), (64, None), (64, "7")])
+def test_layer_prefetch_is_bitwise_neutral(dev, layer, M, mask, monkeypatch):
+    """Every prefetch choice (default policy, or all of them forced) leaves results bit-identical."""
+    if mask is not None:
+        monkeypatch.setenv("HLA_PREFETCH_MASK", mask)
     w, L, p = layer
-    M = 8
-    x = inputs.activations(M, FULL["Hd"], inputs.generator(4100)).to(dev)
+    x = inputs.activations(M, FULL["Hd"], inputs.generator(4100 + M)).to(dev)
     S0 = warm_states(4, M, H, D)
     S1, S2 = S0.to(dev), S0.to(dev)
     y1 = _run(dev, L, M, x, S1)
     y2 = _run(dev, L, M, x, S2, prefetch=True)
     torch.cuda.synchronize()
-    assert hla.hla_last_variant() == "decode_layer<prefetch>"
     assert torch.equal(y1, y2) and torch.equal(S1, S2)
 
 
-def test_layer_in_cuda_graph_matches_eager(dev, layer):
+@pytest.mark.parametrize("M", [8, 64])
+def test_layer_in_cuda_graph_matches_eager(dev, layer, M):
+    """Captured with its prefetch stream (at batch 64 the side-stream fork/join is captured too)."""
     w, L, p = layer
-    M = 8
-    x = inputs.activations(M, FULL["Hd"], inputs.generator(4200)).to(dev)
+    x = inputs.activations(M, FULL["Hd"], inputs.generator(4200 + M)).to(dev)
     S0 = warm_states(4, M, H, D)
     S_eager = S0.to(dev)
-    y_eager = _run(dev, L, M, x, S_eager)
+    y_eager = _run(dev, L, M, x, S_eager, prefetch=True)
     S_graph = S0.to(dev)
     y = torch.empty(M, FULL["Hd"], dtype=torch.bfloat16, device=dev)
     nb = hla.hla_decode_layer_workspace_size(L, M)

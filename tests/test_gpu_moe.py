@@ -189,6 +189,39 @@ def test_tiny_moe(dev, n_shared):
     assert frob_rel(f64(y), y_ref) < MOE_FROB_REL
 
 
+@pytest.mark.parametrize("M,ks", [(20, "0"), (20, "3"), (40, "0")])
+def test_shared_experts_on_tensor_core_path(dev, M, ks, monkeypatch):
+    """With HLA_SHARED_TC=1, past 16 tokens the shared experts run as dense SwiGLU products on
+    tcgen05 (not as grouped work units); with a forced K split of the routed gate/up the two
+    paths coexist."""
+    monkeypatch.setenv("HLA_SHARED_TC", "1")
+    if ks != "0":
+        monkeypatch.setenv("HLA_MOE_SPLIT", ks)
+    Hd, I, E, k, ns = 256, 128, 16, 2, 2
+    g = inputs.generator(70 + M)
+    w = inputs.moe_weights(E, Hd, I, ns, g)
+    x, _ = tie_free_activations(M, Hd, f64(w["W_r"]), k, 70 + M)
+    wd = {kk: vv.to(dev) for kk, vv in w.items()}
+    idx_ref, w_ref, _ = oracle.moe.route_topk(f64(x), f64(w["W_r"]), k)
+    idx = torch.from_numpy(idx_ref.astype("int32")).to(dev)
+    wt = torch.from_numpy(w_ref.astype("float32")).to(dev)
+    res = inputs.activations(M, Hd, g).to(dev)
+    y = torch.empty(M, Hd, dtype=torch.bfloat16, device=dev)
+    nb = hla.moe_expert_forward_workspace_size(M, Hd, I, E, k, ns)
+    ws = _ws(nb, dev)
+    hla.moe_expert_forward(M, Hd, I, E, k, ns, x.to(dev), idx, wt, wd["W_gate"], wd["W_up"],
+                           wd["W_down"], wd["Ws_gate"], wd["Ws_up"], wd["Ws_down"], res, y, ws, nb)
+    variant = hla.hla_last_variant()
+    torch.cuda.synchronize()
+    assert "shared_tc" in variant and (ks == "0" or f"ks{ks}" in variant), variant
+    assert hla.hla_device_status() == 0
+    shared = [(f64(w["Ws_gate"][s]), f64(w["Ws_up"][s]), f64(w["Ws_down"][s])) for s in range(ns)]
+    y_ref = oracle.moe.moe_forward(f64(x), idx_ref, w_ref,
+                                   (f64(w["W_gate"]), f64(w["W_up"]), f64(w["W_down"])), shared,
+                                   residual=f64(res))
+    assert frob_rel(f64(y), y_ref) < MOE_FROB_REL
+
+
 # ----------------------------------------------------------------------------- full-size MoE
 
 def _run_moe(dev, w, x, idx, wt, residual=None, prefetch=False):
