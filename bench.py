@@ -618,6 +618,48 @@ def run_profile(kind, iters=3):
     print(json.dumps(info))
 
 
+# ----------------------------------------------------------------------------- prefetch A/B
+
+def run_prefetch_ab(reps=4):
+    """Layer time at batch 1 / 8 / 64 for every side-stream prefetch mask (interleaved
+    repetitions, CUDA graph of 8 calls each), with clocks; one JSON line."""
+    import torch
+    from hybrid_linear_attention_gated_gb300 import build, hla, inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    wl = Workload(dev, 0, prefetch=True)
+    c = CFG
+    masks = ["none", "0", "1", "2", "3", "7"]
+    sampler = ClockSampler(0)
+    sampler.start()
+    table = {}
+    for M in (1, 8, 64):
+        g = inputs.generator(9000 + M, dev)
+        xs = [inputs.activations(M, c["Hd"], g, dev) for _ in range(ROTATE)]
+        S = wl.S[:M].clone()
+        y = torch.empty(M, c["Hd"], dtype=torch.bfloat16, device=dev)
+        nb = hla.hla_decode_layer_workspace_size(wl.L, M)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        res = {m: [] for m in masks}
+        for _ in range(reps):
+            for m in masks:
+                os.environ.pop("HLA_PREFETCH_MASK", None)
+                if m != "none":
+                    os.environ["HLA_PREFETCH_MASK"] = m
+                pf = 0 if m == "none" else wl.side
+
+                def fn(i, pf=pf):
+                    hla.hla_decode_layer(wl.L, M, xs[i % ROTATE], S, None, y, ws, nb, prefetch_stream=pf)
+                res[m].append(graph_time(torch, fn, 8) * 1e6)
+        os.environ.pop("HLA_PREFETCH_MASK", None)
+        table[M] = {m: round(statistics.median(v), 1) for m, v in res.items()}
+    clocks = sampler.stop()
+    print(json.dumps({"prefetch_ab_us_per_layer": table, "clocks": clocks,
+                      "masks": "none = no prefetch stream; 1 = W_o+W_r during KDA; 2 = shared gate/up "
+                               "during dispatch; 4 = shared down"}))
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -705,9 +747,13 @@ def main():
     ap.add_argument("--no-prefetch", action="store_true")
     ap.add_argument("--profile", choices=["moe", "kda", "dense"],
                     help="run one small case of a hot kernel (for ncu captures) and exit")
+    ap.add_argument("--prefetch-ab", action="store_true",
+                    help="time the layer under every side-stream prefetch mask and exit")
     args = ap.parse_args()
     if args.profile:
         return run_profile(args.profile)
+    if args.prefetch_ab:
+        return run_prefetch_ab()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
