@@ -338,6 +338,45 @@ def moe_sweep(torch, hla, inputs, wl, dev, peak):
     return res
 
 
+def spec_sweep(torch, hla, inputs, wl, dev, peak):
+    """Speculative window at B=16, T=4 (accepted length uniform in 0..4), two forms per step:
+    separate (verify + accept + replay) and fused (replay of the previous window with the
+    verify of the next + accept).  Each step rotates through 4 windows."""
+    c = CFG
+    B, T, H, d = c["spec_B"], c["spec_T"], c["H"], c["d"]
+    S = wl.S_spec.clone()
+    o = torch.empty(B, T, H, d, device=dev)
+    acc = torch.zeros(B, dtype=torch.int32, device=dev)
+    com = torch.zeros(B, dtype=torch.int32, device=dev)
+
+    def separate(i):
+        w = wl.win[i % ROTATE]
+        dr, tg, _ = wl.ids[i % ROTATE]
+        hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, S, None, w["q"], w["k"], w["v"],
+                                   w["alpha"], w["beta"], None, o)
+        hla.spec_accept_prefix(B, T, dr, tg, acc, com)
+        hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, S, None, w["q"], w["k"], w["v"],
+                                   w["alpha"], w["beta"], acc, None)
+
+    def fused(i):
+        p_, w = wl.win[(i + ROTATE - 1) % ROTATE], wl.win[i % ROTATE]
+        dr, tg, _ = wl.ids[i % ROTATE]
+        hla.kda_spec_replay_verify(B, T, T, H, d, d, S, None, p_["q"], p_["k"], p_["v"], p_["alpha"],
+                                   p_["beta"], acc, w["q"], w["k"], w["v"], w["alpha"], w["beta"], o)
+        hla.spec_accept_prefix(B, T, dr, tg, acc, com)
+    res = []
+    mean_sep = statistics.mean(sum(spec_bytes(B, T, wl.ids[r][2]).values()) for r in range(ROTATE))
+    tok = 3 * d * 2 + d * 4 + 4
+    mean_fused = statistics.mean(
+        B * H * 4 * d * d + sum(H * (4 * d * d + int(a) * tok) for a in wl.ids[r][2] if a > 0)
+        + B * H * T * (tok + 4 * d) + 2 * B * T * 4 + 3 * B * 4 for r in range(ROTATE))
+    for name, fn, nbytes in (("separate", separate, mean_sep), ("fused", fused, mean_fused)):
+        t = graph_time(torch, fn, 4 * ROTATE)
+        res.append(dict(form=name, us=round(t * 1e6, 2), bytes=round(nbytes),
+                        gbs=round(nbytes / t / 1e9, 1), frac=round(nbytes / t / 1e9 / peak, 3)))
+    return res
+
+
 def layer_sweep(torch, hla, inputs, wl, dev, peak):
     c = CFG
     res = []
@@ -498,6 +537,7 @@ def run_ours(args):
         sweeps["kda_decode"] = kda_sweep(torch, hla, inputs, dev, peak)
         sweeps["moe"] = moe_sweep(torch, hla, inputs, wl, dev, peak)
         sweeps["layer"] = layer_sweep(torch, hla, inputs, wl, dev, peak)
+        sweeps["spec_window"] = spec_sweep(torch, hla, inputs, wl, dev, peak)
     clocks = sampler.stop()
 
     if rank != 0:

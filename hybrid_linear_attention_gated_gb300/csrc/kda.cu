@@ -28,19 +28,26 @@ namespace {
 constexpr int kRowGroups = 8;
 constexpr int kMaxWindow = 8;
 
-enum KdaMode { kDecode = 0, kVerify = 1, kReplay = 2 };
+enum KdaMode { kDecode = 0, kVerify = 1, kReplay = 2, kReplayVerify = 3 };
 
 struct KdaParams {
     float *S;
     const int32_t *state_idx;
-    const uint16_t *q, *k, *v;
+    const uint16_t *q, *k, *v;          // this call's tokens [B, T, H, .] (T = 1 for decode)
     const float *alpha, *beta;
-    const int32_t *accepted;
+    const uint16_t *qp, *kp, *vp;       // replay-verify: the previous window [B, Tp, H, .]
+    const float *alphap, *betap;
+    const int32_t *accepted;            // replay: of this window; replay-verify: of the previous one
     void *o;
     int o_bf16;
-    int B, T, H;
+    int B, T, Tp, H;
 };
 
+// Each CTA runs a short program over its (sequence, head, column slice):
+//   n_pre steps from the previous window, then commit the state (replay-verify only);
+//   n_main steps from this call's tokens, writing o (decode, verify, replay-verify) and/or
+//   committing the state at the end (decode, replay).
+// Every step is the same arithmetic, so any combination is bit-identical to the separate calls.
 template <int DK, int CW, int MODE>
 __global__ void __launch_bounds__(kRowGroups *CW / 4)
     kda_recur_kernel(const KdaParams p) {
@@ -49,7 +56,8 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
     constexpr int DV = DK;
     constexpr int NSLICE = DV / CW;
     constexpr int NTHR = kRowGroups * CG;
-    constexpr int TMAX = MODE == kDecode ? 1 : kMaxWindow;
+    constexpr int TMAX = MODE == kDecode ? 1 : (MODE == kReplayVerify ? 2 * kMaxWindow : kMaxWindow);
+    constexpr bool WRITE_O = MODE != kReplay;
 
     __shared__ float sq[TMAX][DK], sk[TMAX][DK], sa[TMAX][DK], sv[TMAX][CW], sb[TMAX];
     __shared__ float4 red_u[2][kRowGroups][CG], red_w[2][kRowGroups][CG];
@@ -64,12 +72,19 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
     const int b = bh / p.H;
     const int col0 = slice * CW;
 
-    int steps = MODE == kDecode ? 1 : p.T;
-    if (MODE == kReplay) {
-        const int a = p.accepted[b];
-        steps = a < 0 ? 0 : (a > p.T ? p.T : a);
-        if (steps == 0) return;  // nothing accepted: the committed state is not touched
+    int n_pre = 0, n_main = MODE == kDecode ? 1 : p.T;
+    if (MODE == kReplay || MODE == kReplayVerify) {
+        const int lim = MODE == kReplay ? p.T : p.Tp;
+        const int a0 = p.accepted[b];
+        const int a = a0 < 0 ? 0 : (a0 > lim ? lim : a0);
+        if (MODE == kReplay) {
+            n_main = a;
+            if (a == 0) return;  // nothing accepted: the committed state is not touched
+        } else {
+            n_pre = a;
+        }
     }
+    const int steps = n_pre + n_main;
 
     const int slot = p.state_idx ? p.state_idx[b] : b;
     float *Sb = p.S + ((size_t)slot * p.H + h) * (size_t)(DK * DV) + col0 + cg * 4;
@@ -79,17 +94,21 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
     for (int j = 0; j < RPT; ++j)
         s[j] = *reinterpret_cast<const float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV);
 
-    // the window's per-token vectors (token t of sequence b is row (b*T + t) of [B, T, H, .])
+    // per-token vectors: token t of sequence b is row (b*T + t) of its [B, T, H, .] tensor
     const int Tld = MODE == kDecode ? 1 : p.T;
     for (int t = 0; t < steps; ++t) {
-        const size_t tok = ((size_t)b * Tld + t) * p.H + h;
+        const bool pre = t < n_pre;
+        const uint16_t *q = pre ? p.qp : p.q, *k = pre ? p.kp : p.k, *v = pre ? p.vp : p.v;
+        const float *al = pre ? p.alphap : p.alpha, *be = pre ? p.betap : p.beta;
+        const size_t tok = pre ? ((size_t)b * p.Tp + t) * p.H + h
+                               : ((size_t)b * Tld + (t - n_pre)) * p.H + h;
         for (int i = tid; i < DK; i += NTHR) {
-            sq[t][i] = bf16_bits_to_float(p.q[tok * DK + i]);
-            sk[t][i] = bf16_bits_to_float(p.k[tok * DK + i]);
-            sa[t][i] = p.alpha[tok * DK + i];
+            sq[t][i] = bf16_bits_to_float(q[tok * DK + i]);
+            sk[t][i] = bf16_bits_to_float(k[tok * DK + i]);
+            sa[t][i] = al[tok * DK + i];
         }
-        for (int c = tid; c < CW; c += NTHR) sv[t][c] = bf16_bits_to_float(p.v[tok * DV + col0 + c]);
-        if (tid == 0) sb[t] = p.beta[tok];
+        for (int c = tid; c < CW; c += NTHR) sv[t][c] = bf16_bits_to_float(v[tok * DV + col0 + c]);
+        if (tid == 0) sb[t] = be[tok];
     }
     __syncthreads();
 
@@ -145,13 +164,13 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
             s[j].z = __fmaf_rn(kk, d.z, s[j].z);
             s[j].w = __fmaf_rn(kk, d.w, s[j].w);
         }
-        if (MODE != kReplay && rg == 0) {
+        if (WRITE_O && t >= n_pre && rg == 0) {
             float4 o;
             o.x = __fmaf_rn(qk, d.x, w.x);
             o.y = __fmaf_rn(qk, d.y, w.y);
             o.z = __fmaf_rn(qk, d.z, w.z);
             o.w = __fmaf_rn(qk, d.w, w.w);
-            const size_t oo = (((size_t)b * Tld + t) * p.H + h) * DV + col0 + cg * 4;
+            const size_t oo = (((size_t)b * Tld + (t - n_pre)) * p.H + h) * DV + col0 + cg * 4;
             if (p.o_bf16) {
                 uint2 pk = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
                 *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.o) + oo) = pk;
@@ -159,9 +178,15 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
                 *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + oo) = o;
             }
         }
+        if (MODE == kReplayVerify && t + 1 == n_pre) {
+            // the replayed prefix is the new committed state; the new window is only verified
+#pragma unroll
+            for (int j = 0; j < RPT; ++j)
+                *reinterpret_cast<float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV) = s[j];
+        }
     }
 
-    if (MODE != kVerify) {
+    if (MODE == kDecode || MODE == kReplay) {
 #pragma unroll
         for (int j = 0; j < RPT; ++j)
             *reinterpret_cast<float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV) = s[j];
@@ -178,7 +203,7 @@ int launch_dk(int cw, const KdaParams &p, cudaStream_t st) {
         case 32: kda_recur_kernel<DK, 32, MODE><<<grid, kRowGroups * 8, 0, st>>>(p); break;
         case 64: kda_recur_kernel<DK, 64, MODE><<<grid, kRowGroups * 16, 0, st>>>(p); break;
         case 128:
-            if constexpr (DK >= 128) {
+            if constexpr (DK >= 128 && MODE != kReplayVerify) {
                 kda_recur_kernel<DK, 128, MODE><<<grid, kRowGroups * 32, 0, st>>>(p);
                 break;
             } else {
@@ -206,17 +231,32 @@ int choose_cw(int B, int H, int dv) {
     return cw;
 }
 
+struct PrevWindow {
+    const hla_bf16 *q = nullptr, *k = nullptr, *v = nullptr;
+    const float *alpha = nullptr, *beta = nullptr;
+    int T = 0;
+};
+
 int run_kda(int mode, int B, int T, int H, int dk, int dv, float *S, const int32_t *state_idx,
             const hla_bf16 *q, const hla_bf16 *k, const hla_bf16 *v, const float *alpha,
-            const float *beta, const int32_t *accepted, void *o, int o_dtype, cudaStream_t st) {
+            const float *beta, const int32_t *accepted, void *o, int o_dtype, cudaStream_t st,
+            const PrevWindow &prev = PrevWindow()) {
     HLA_REQUIRE(B >= 1 && H >= 1 && T >= 1, HLA_ERR_INVALID_ARG);
     HLA_REQUIRE(dk == dv && (dk == 64 || dk == 128), HLA_ERR_UNSUPPORTED);
     HLA_REQUIRE(T <= kMaxWindow, HLA_ERR_UNSUPPORTED);
     HLA_REQUIRE((long)B * H * (dv / 16) < (1L << 31), HLA_ERR_UNSUPPORTED);
     HLA_REQUIRE(S && q && k && v && alpha && beta, HLA_ERR_INVALID_ARG);
-    HLA_REQUIRE(mode != kReplay || accepted, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE((mode != kReplay && mode != kReplayVerify) || accepted, HLA_ERR_INVALID_ARG);
     HLA_REQUIRE(mode == kReplay || o, HLA_ERR_INVALID_ARG);
     HLA_REQUIRE(o_dtype == HLA_F32 || o_dtype == HLA_BF16, HLA_ERR_INVALID_ARG);
+    if (mode == kReplayVerify) {
+        HLA_REQUIRE(prev.T >= 1, HLA_ERR_INVALID_ARG);
+        HLA_REQUIRE(prev.T <= kMaxWindow, HLA_ERR_UNSUPPORTED);
+        HLA_REQUIRE(prev.q && prev.k && prev.v && prev.alpha && prev.beta, HLA_ERR_INVALID_ARG);
+        HLA_REQUIRE(aligned16(prev.q) && aligned16(prev.k) && aligned16(prev.v) &&
+                        aligned16(prev.alpha) && aligned16(prev.beta),
+                    HLA_ERR_MISALIGNED);
+    }
     HLA_REQUIRE(aligned16(S) && aligned16(q) && aligned16(k) && aligned16(v) && aligned16(alpha) &&
                     aligned16(beta) && (o == nullptr || aligned16(o)) &&
                     (state_idx == nullptr || aligned16(state_idx)) &&
@@ -224,19 +264,24 @@ int run_kda(int mode, int B, int T, int H, int dk, int dv, float *S, const int32
                 HLA_ERR_MISALIGNED);
     KdaParams p;
     p.S = S; p.state_idx = state_idx; p.q = q; p.k = k; p.v = v; p.alpha = alpha; p.beta = beta;
+    p.qp = prev.q; p.kp = prev.k; p.vp = prev.v; p.alphap = prev.alpha; p.betap = prev.beta;
+    p.Tp = prev.T;
     p.accepted = accepted; p.o = o; p.o_bf16 = o_dtype == HLA_BF16; p.B = B; p.T = T; p.H = H;
-    const int cw = choose_cw(B, H, dv);
-    static const char *names[3] = {"decode", "verify", "replay"};
+    int cw = choose_cw(B, H, dv);
+    if (mode == kReplayVerify && cw > 64) cw = 64;  // two windows of token vectors in shared memory
+    static const char *names[4] = {"decode", "verify", "replay", "replay_verify"};
     set_variant("kda_recur<dk%d,cw%d,%s>", dk, cw, names[mode]);
     int st_ = HLA_ERR_UNSUPPORTED;
     if (dk == 128) {
         st_ = mode == kDecode ? launch_dk<128, kDecode>(cw, p, st)
             : mode == kVerify ? launch_dk<128, kVerify>(cw, p, st)
-                              : launch_dk<128, kReplay>(cw, p, st);
+            : mode == kReplay ? launch_dk<128, kReplay>(cw, p, st)
+                              : launch_dk<128, kReplayVerify>(cw, p, st);
     } else {
         st_ = mode == kDecode ? launch_dk<64, kDecode>(cw, p, st)
             : mode == kVerify ? launch_dk<64, kVerify>(cw, p, st)
-                              : launch_dk<64, kReplay>(cw, p, st);
+            : mode == kReplay ? launch_dk<64, kReplay>(cw, p, st)
+                              : launch_dk<64, kReplayVerify>(cw, p, st);
     }
     return st_;
 }
@@ -277,6 +322,20 @@ extern "C" int kda_spec_verify_replay(int phase, int B, int T, int H, int dk, in
         return run_kda(kReplay, B, T, H, dk, dv, S, state_idx, q, k, v, alpha, beta,
                        accepted_len, nullptr, o_dtype, (cudaStream_t)stream);
     return HLA_ERR_INVALID_ARG;
+}
+
+extern "C" int kda_spec_replay_verify(int B, int T_prev, int T, int H, int dk, int dv, float *S,
+                                      const int32_t *state_idx, const hla_bf16 *q_prev,
+                                      const hla_bf16 *k_prev, const hla_bf16 *v_prev,
+                                      const float *alpha_prev, const float *beta_prev,
+                                      const int32_t *accepted_prev, const hla_bf16 *q,
+                                      const hla_bf16 *k, const hla_bf16 *v, const float *alpha,
+                                      const float *beta, void *o, int o_dtype, hla_stream stream) {
+    PrevWindow prev;
+    prev.q = q_prev; prev.k = k_prev; prev.v = v_prev; prev.alpha = alpha_prev; prev.beta = beta_prev;
+    prev.T = T_prev;
+    return run_kda(kReplayVerify, B, T, H, dk, dv, S, state_idx, q, k, v, alpha, beta, accepted_prev,
+                   o, o_dtype, (cudaStream_t)stream, prev);
 }
 
 extern "C" int spec_accept_prefix(int B, int T, const int32_t *draft_ids,

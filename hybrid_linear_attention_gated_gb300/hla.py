@@ -48,6 +48,7 @@ SIGNATURES = {
     "kda_decode_step": (c_int, [c_int] * 4 + [P] * 8 + [c_int, P]),
     "kda_spec_verify_replay": (c_int, [c_int] * 6 + [P] * 9 + [c_int, P]),
     "spec_accept_prefix": (c_int, [c_int, c_int] + [P] * 4 + [P]),
+    "kda_spec_replay_verify": (c_int, [c_int] * 6 + [P] * 14 + [c_int, P]),
     "skinny_proj_splitk_workspace_size": (c_size_t, [c_int] * 4),
     "skinny_proj_splitk": (c_int, [c_int] * 3 + [P] * 4 + [c_int, c_int, P, c_size_t, P]),
     "kda_qkvg_proj_workspace_size": (c_size_t, [c_int] * 6),
@@ -142,6 +143,15 @@ def kda_spec_verify_replay(phase, B, T, H, dk, dv, S, state_idx, q, k, v, alpha,
     return _check("kda_spec_verify_replay", load().kda_spec_verify_replay(
         phase, B, T, H, dk, dv, _p(S), _p(state_idx), _p(q), _p(k), _p(v), _p(alpha), _p(beta),
         _p(accepted_len), _p(o), o_dtype, _stream(stream)))
+
+
+def kda_spec_replay_verify(B, T_prev, T, H, dk, dv, S, state_idx, q_prev, k_prev, v_prev,
+                           alpha_prev, beta_prev, accepted_prev, q, k, v, alpha, beta, o,
+                           o_dtype=HLA_F32, stream=None):
+    return _check("kda_spec_replay_verify", load().kda_spec_replay_verify(
+        B, T_prev, T, H, dk, dv, _p(S), _p(state_idx), _p(q_prev), _p(k_prev), _p(v_prev),
+        _p(alpha_prev), _p(beta_prev), _p(accepted_prev), _p(q), _p(k), _p(v), _p(alpha), _p(beta),
+        _p(o), o_dtype, _stream(stream)))
 
 
 def spec_accept_prefix(B, T, draft_ids, target_ids, accepted_len, committed_len, stream=None):

@@ -130,6 +130,29 @@ int kda_spec_verify_replay(int phase, int B, int T, int H, int dk, int dv, float
                            hla_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * Replay of the previous window fused with the verify of the next one.  [KIMI-WEBINAR]
+ * speculative decoding: only the accepted portion of the last window is replayed from the
+ * last committed state, and the next drafted window is verified from the new committed
+ * state.  One pass over the state does both, so each (sequence, head) state is read once
+ * and written once per speculative step instead of read twice.
+ *  For every (b, h): from S[slot(b), h] apply the first a = accepted_prev[b] tokens of the
+ *  previous window (clamped to [0, T_prev]); if a > 0 store the result as the committed state;
+ *  then apply the T tokens of the new window to a private copy and write o[b, t, h] for every t
+ *  (the new window is not committed).
+ *  q_prev, k_prev [B, T_prev, H, dk] bf16, v_prev [B, T_prev, H, dv] bf16, alpha_prev fp32
+ *  [B, T_prev, H, dk], beta_prev fp32 [B, T_prev, H]; accepted_prev int32 [B]; the new window
+ *  q, k, v, alpha, beta with T in place of T_prev; o [B, T, H, dv] (o_dtype).
+ *  1 <= T_prev, T <= 8.  Bit-identical to kda_spec_verify_replay(REPLAY) on the previous window
+ *  followed by kda_spec_verify_replay(VERIFY) on the new one.
+ * -------------------------------------------------------------------------*/
+int kda_spec_replay_verify(int B, int T_prev, int T, int H, int dk, int dv, float *S,
+                           const int32_t *state_idx, const hla_bf16 *q_prev, const hla_bf16 *k_prev,
+                           const hla_bf16 *v_prev, const float *alpha_prev, const float *beta_prev,
+                           const int32_t *accepted_prev, const hla_bf16 *q, const hla_bf16 *k,
+                           const hla_bf16 *v, const float *alpha, const float *beta, void *o,
+                           int o_dtype, hla_stream stream);
+
+/* ---------------------------------------------------------------------------
  * Accepted-length bookkeeping.  [KIMI-WEBINAR] speculative decoding: greedy
  * acceptance of the drafted tokens the target agrees with.
  *  accepted_len[b]  = number of leading t with draft_ids[b,t] == target_ids[b,t]

@@ -120,3 +120,15 @@ def spec_replay(S_c, q, k, v, alpha, beta, accepted_len):
         for t in range(int(accepted_len[b])):
             S[b], _ = kda_step(S[b], q[b, t], k[b, t], v[b, t], alpha[b, t], beta[b, t])
     return S
+
+
+def spec_replay_verify(S_c, prev, accepted_prev, new):
+    """One speculative step in fused form: commit the accepted prefix of the previous window,
+    then verify the new window from the new committed state.
+
+    prev / new: dicts of q, k, v, alpha, beta with the draft axis at 1.  Returns
+    (new committed states [B, H, d_k, d_v], outputs of the new window [B, T, H, d_v]).
+    """
+    S = spec_replay(S_c, prev["q"], prev["k"], prev["v"], prev["alpha"], prev["beta"], accepted_prev)
+    o = spec_verify(S, new["q"], new["k"], new["v"], new["alpha"], new["beta"])
+    return S, o

@@ -372,3 +372,49 @@ def layer_pin_failures(qkvg_epilogue, decode_layer, step, rmsnorm, round_bf16):
     if not (np.allclose(S_new, S_ref, rtol=1e-14, atol=1e-14) and np.allclose(aux["o"], o_ref, rtol=1e-14, atol=1e-14)):
         fails.append("layer KDA composition")
     return sorted(set(fails))
+
+
+# --------------------------------------------------------------------------------------
+# fused replay (previous window) + verify (next window)
+# --------------------------------------------------------------------------------------
+
+def fused_pin_failures(step, replay_verify):
+    fails = []
+    # hand-worked chain: previous window = golden example 1 accepted (a = 1), next window =
+    # golden example 3 -> committed state = example 1's S_t, next output = example 3's o
+    exs = _load("kda_worked_examples.json")["examples"]
+    e1, e3 = exs[0], exs[2]
+    win = lambda e: {key: np.array([[[e[key]]]], float) for key in ("q", "k", "v", "alpha")}  # noqa: E731
+    prev, new = win(e1), win(e3)
+    prev["beta"] = np.array([[[e1["beta"]]]], float)
+    new["beta"] = np.array([[[e3["beta"]]]], float)
+    S_c = np.array([[e1["S"]]], float)
+    S_new, o = replay_verify(S_c, prev, np.array([1]), new)
+    if not (np.array_equal(S_new[0, 0], np.array(e1["S_t"], float))
+            and np.array_equal(o[0, 0, 0], np.array(e3["o"], float))):
+        fails.append("fused golden chain")
+    S_new, o = replay_verify(S_c, prev, np.array([0]), new)
+    if not np.array_equal(S_new[0, 0], np.array(e1["S"], float)):
+        fails.append("fused with nothing accepted keeps the committed state")
+
+    # brute force against sequential steps, windows of different lengths
+    rng = _rng(21)
+    B, Tp, T, H, dk, dv = 3, 3, 2, 2, 4, 3
+    S_c = rng.standard_normal((B, H, dk, dv))
+    mk = lambda n: dict(q=rng.standard_normal((B, n, H, dk)), k=rng.standard_normal((B, n, H, dk)),  # noqa: E731
+                        v=rng.standard_normal((B, n, H, dv)), alpha=rng.uniform(0.1, 0.9, (B, n, H, dk)),
+                        beta=rng.uniform(0, 1, (B, n, H)))
+    prev, new = mk(Tp), mk(T)
+    acc = np.array([0, 2, 3])
+    S_new, o = replay_verify(S_c, prev, acc, new)
+    for b in range(B):
+        S = S_c[b].copy()
+        for t in range(acc[b]):
+            S, _ = step(S, prev["q"][b, t], prev["k"][b, t], prev["v"][b, t], prev["alpha"][b, t], prev["beta"][b, t])
+        if not np.allclose(S, S_new[b], rtol=1e-13, atol=1e-13):
+            fails.append("fused committed state equals sequential accepted steps")
+        for t in range(T):
+            S, ot = step(S, new["q"][b, t], new["k"][b, t], new["v"][b, t], new["alpha"][b, t], new["beta"][b, t])
+            if not np.allclose(ot, o[b, t], rtol=1e-13, atol=1e-13):
+                fails.append("fused outputs equal sequential steps from the new committed state")
+    return sorted(set(fails))

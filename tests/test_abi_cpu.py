@@ -38,6 +38,32 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(hla.SIGNATURES) == set(declared_functions())
 
 
+def declared_signatures():
+    """name -> list of parameter type strings, parsed from include/hla.h."""
+    src = open(os.path.join(ROOT, "include", "hla.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"#.*", "", src)
+    out = {}
+    for m in re.finditer(r"([A-Za-z_][\w \*]*?)\b([a-z_][a-z0-9_]*)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
+        params = [p.strip() for p in m.group(3).split(",")]
+        out[m.group(2)] = [] if params == ["void"] or params == [""] else params
+    return out
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every ctypes signature has the header's parameter count, and pointer parameters are
+    marshalled as pointers (a pointer passed as int would be truncated)."""
+    sigs = declared_signatures()
+    assert set(sigs) == set(hla.SIGNATURES)
+    for name, params in sigs.items():
+        _, argtypes = hla.SIGNATURES[name]
+        assert len(argtypes) == len(params), name
+        for decl, at in zip(params, argtypes):
+            is_ptr = "*" in decl or decl.startswith("hla_stream")
+            assert is_ptr == (at is not ctypes.c_int and at is not ctypes.c_float and
+                              at is not ctypes.c_size_t), (name, decl, at)
+
+
 def test_built_for_sm103a_only(lib):
     assert "arch=compute_103a,code=sm_103a" in " ".join(build.ARCH)
 

@@ -192,3 +192,44 @@ def test_run_to_run_determinism(dev):
         outs.append(ov)
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("B,Tp,T,d,acc_kind", [(16, 4, 4, 128, "uniform"), (4, 3, 5, 128, "zero"),
+                                                (4, 8, 8, 128, "all"), (2, 4, 2, 64, "uniform")])
+def test_fused_replay_verify(dev, B, Tp, T, d, acc_kind):
+    """Replay of the previous window + verify of the next in one pass over the state:
+    bit-identical to the two separate calls, and within tolerance of the oracle."""
+    H = 32 if d == 128 else 4
+    S0 = warm_states(6, B, H, d)
+    g = inputs.generator(600 + B + Tp + T)
+    prev = inputs.kda_inputs((B, Tp), H, d, d, g)
+    new = inputs.kda_inputs((B, T), H, d, d, g)
+    if acc_kind == "uniform":
+        _, _, acc = inputs.accept_ids(B, Tp, g)
+    elif acc_kind == "zero":
+        acc = torch.zeros(B, dtype=torch.int64)
+    else:
+        acc = torch.full((B,), Tp, dtype=torch.int64)
+    accd = acc.to(torch.int32).to(dev)
+    pd, nd = _to(prev, dev), _to(new, dev)
+    # fused
+    S1 = S0.to(dev)
+    o1 = torch.empty(B, T, H, d, device=dev)
+    hla.kda_spec_replay_verify(B, Tp, T, H, d, d, S1, None, pd["q"], pd["k"], pd["v"], pd["alpha"],
+                               pd["beta"], accd, nd["q"], nd["k"], nd["v"], nd["alpha"], nd["beta"], o1)
+    assert "replay_verify" in hla.hla_last_variant()
+    # separate
+    S2 = S0.to(dev)
+    o2 = torch.empty(B, T, H, d, device=dev)
+    hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, Tp, H, d, d, S2, None, pd["q"], pd["k"], pd["v"],
+                               pd["alpha"], pd["beta"], accd, None)
+    hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, S2, None, nd["q"], nd["k"], nd["v"],
+                               nd["alpha"], nd["beta"], None, o2)
+    torch.cuda.synchronize()
+    assert torch.equal(S1, S2) and torch.equal(o1, o2)
+    S_ref, o_ref = oracle.kda.spec_replay_verify(f64(S0), _np(prev), acc.numpy(), _np(new))
+    assert max_rel(f64(S1), S_ref) < KDA_MAX_REL
+    assert max_rel(f64(o1), o_ref) < KDA_MAX_REL
+    for b in range(B):
+        if int(acc[b]) == 0:
+            assert torch.equal(S1[b].cpu(), S0[b])

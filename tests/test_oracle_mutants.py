@@ -10,7 +10,7 @@ import pytest
 from oracle import kda, moe, layer, numerics
 from oracle.numerics import f64, sigmoid, silu
 from tests.oracle_pins import (kda_pin_failures, spec_pin_failures, moe_pin_failures,
-                               layer_pin_failures)
+                               layer_pin_failures, fused_pin_failures)
 
 
 def _caught(fn, *args):
@@ -229,3 +229,19 @@ def _epilogue_variant(kind):
 def test_layer_epilogue_mutants_are_caught(kind):
     assert _caught(layer_pin_failures, _epilogue_variant(kind), layer.decode_layer, kda.kda_step,
                    moe.rmsnorm, numerics.round_bf16)
+
+
+def _fused_verifies_stale_state(S_c, prev, acc, new):
+    S = kda.spec_replay(S_c, prev["q"], prev["k"], prev["v"], prev["alpha"], prev["beta"], acc)
+    o = kda.spec_verify(S_c, new["q"], new["k"], new["v"], new["alpha"], new["beta"])
+    return S, o
+
+
+def _fused_replays_all(S_c, prev, acc, new):
+    full = np.full_like(np.asarray(acc), prev["q"].shape[1])
+    return kda.spec_replay_verify(S_c, prev, full, new)
+
+
+@pytest.mark.parametrize("mutant", [_fused_verifies_stale_state, _fused_replays_all])
+def test_fused_mutants_are_caught(mutant):
+    assert _caught(fused_pin_failures, kda.kda_step, mutant)

@@ -5,7 +5,7 @@ import numpy as np
 import oracle
 from oracle import kda, moe, layer, numerics
 from tests.oracle_pins import (kda_pin_failures, spec_pin_failures, moe_pin_failures,
-                               layer_pin_failures)
+                               layer_pin_failures, fused_pin_failures)
 
 
 def test_kda_step_pins():
@@ -14,6 +14,10 @@ def test_kda_step_pins():
 
 def test_spec_window_pins():
     assert spec_pin_failures(kda.kda_step, kda.spec_verify, kda.accept_prefix, kda.spec_replay) == []
+
+
+def test_fused_replay_verify_pins():
+    assert fused_pin_failures(kda.kda_step, kda.spec_replay_verify) == []
 
 
 def test_moe_pins():
