@@ -339,41 +339,53 @@ def moe_sweep(torch, hla, inputs, wl, dev, peak):
 
 
 def spec_sweep(torch, hla, inputs, wl, dev, peak):
-    """Speculative window at B=16, T=4 (accepted length uniform in 0..4), two forms per step:
-    separate (verify + accept + replay) and fused (replay of the previous window with the
-    verify of the next + accept).  Each step rotates through 4 windows."""
+    """Speculative window, T=4, accepted length uniform in 0..4, at B=16 (33.5 MB of committed
+    state: fits in L2) and B=64 (134 MB: does not), two forms per step: separate (verify +
+    accept + replay) and fused (replay of the previous window with the verify of the next +
+    accept).  Each step rotates through 4 windows."""
     c = CFG
-    B, T, H, d = c["spec_B"], c["spec_T"], c["H"], c["d"]
-    S = wl.S_spec.clone()
-    o = torch.empty(B, T, H, d, device=dev)
-    acc = torch.zeros(B, dtype=torch.int32, device=dev)
-    com = torch.zeros(B, dtype=torch.int32, device=dev)
-
-    def separate(i):
-        w = wl.win[i % ROTATE]
-        dr, tg, _ = wl.ids[i % ROTATE]
-        hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, S, None, w["q"], w["k"], w["v"],
-                                   w["alpha"], w["beta"], None, o)
-        hla.spec_accept_prefix(B, T, dr, tg, acc, com)
-        hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, S, None, w["q"], w["k"], w["v"],
-                                   w["alpha"], w["beta"], acc, None)
-
-    def fused(i):
-        p_, w = wl.win[(i + ROTATE - 1) % ROTATE], wl.win[i % ROTATE]
-        dr, tg, _ = wl.ids[i % ROTATE]
-        hla.kda_spec_replay_verify(B, T, T, H, d, d, S, None, p_["q"], p_["k"], p_["v"], p_["alpha"],
-                                   p_["beta"], acc, w["q"], w["k"], w["v"], w["alpha"], w["beta"], o)
-        hla.spec_accept_prefix(B, T, dr, tg, acc, com)
-    res = []
-    mean_sep = statistics.mean(sum(spec_bytes(B, T, wl.ids[r][2]).values()) for r in range(ROTATE))
+    T, H, d = c["spec_T"], c["H"], c["d"]
     tok = 3 * d * 2 + d * 4 + 4
-    mean_fused = statistics.mean(
-        B * H * 4 * d * d + sum(H * (4 * d * d + int(a) * tok) for a in wl.ids[r][2] if a > 0)
-        + B * H * T * (tok + 4 * d) + 2 * B * T * 4 + 3 * B * 4 for r in range(ROTATE))
-    for name, fn, nbytes in (("separate", separate, mean_sep), ("fused", fused, mean_fused)):
-        t = graph_time(torch, fn, 4 * ROTATE)
-        res.append(dict(form=name, us=round(t * 1e6, 2), bytes=round(nbytes),
-                        gbs=round(nbytes / t / 1e9, 1), frac=round(nbytes / t / 1e9 / peak, 3)))
+    res = []
+    for B in (16, 64):
+        if B == c["spec_B"]:
+            S, wins, ids = wl.S_spec.clone(), wl.win, wl.ids
+        else:
+            g = inputs.generator(7700 + B, dev)
+            S = wl.S[:B].clone()
+            wins, ids = [], []
+            for _ in range(ROTATE):
+                wins.append(inputs.kda_inputs((B, T), H, d, d, g, dev))
+                dr, tg, a = inputs.accept_ids(B, T, g, dev)
+                ids.append((dr, tg, a.cpu().numpy()))
+        o = torch.empty(B, T, H, d, device=dev)
+        acc = torch.zeros(B, dtype=torch.int32, device=dev)
+        com = torch.zeros(B, dtype=torch.int32, device=dev)
+
+        def separate(i, B=B, S=S, wins=wins, ids=ids, o=o, acc=acc, com=com):
+            w = wins[i % ROTATE]
+            dr, tg, _ = ids[i % ROTATE]
+            hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, S, None, w["q"], w["k"],
+                                       w["v"], w["alpha"], w["beta"], None, o)
+            hla.spec_accept_prefix(B, T, dr, tg, acc, com)
+            hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, S, None, w["q"], w["k"],
+                                       w["v"], w["alpha"], w["beta"], acc, None)
+
+        def fused(i, B=B, S=S, wins=wins, ids=ids, o=o, acc=acc, com=com):
+            p_, w = wins[(i + ROTATE - 1) % ROTATE], wins[i % ROTATE]
+            dr, tg, _ = ids[i % ROTATE]
+            hla.kda_spec_replay_verify(B, T, T, H, d, d, S, None, p_["q"], p_["k"], p_["v"],
+                                       p_["alpha"], p_["beta"], acc, w["q"], w["k"], w["v"],
+                                       w["alpha"], w["beta"], o)
+            hla.spec_accept_prefix(B, T, dr, tg, acc, com)
+        mean_sep = statistics.mean(sum(spec_bytes(B, T, ids[r][2]).values()) for r in range(ROTATE))
+        mean_fused = statistics.mean(
+            B * H * 4 * d * d + sum(H * (4 * d * d + int(a) * tok) for a in ids[r][2] if a > 0)
+            + B * H * T * (tok + 4 * d) + 2 * B * T * 4 + 3 * B * 4 for r in range(ROTATE))
+        for name, fn, nbytes in (("separate", separate, mean_sep), ("fused", fused, mean_fused)):
+            t = graph_time(torch, fn, 4 * ROTATE)
+            res.append(dict(batch=B, form=name, us=round(t * 1e6, 2), bytes=round(nbytes),
+                            gbs=round(nbytes / t / 1e9, 1), frac=round(nbytes / t / 1e9 / peak, 3)))
     return res
 
 

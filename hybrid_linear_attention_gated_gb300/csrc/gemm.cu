@@ -21,6 +21,7 @@ int router_split(int M, int Hd, int E);
 namespace {
 
 constexpr int kDenseThreads = 128;  // 4 warps, one item per warp
+constexpr int kNormThreads = 1024;  // RMSNorm kernels: one CTA per row (same layout => same sums)
 
 struct DenseParams {
     const uint16_t *W;
@@ -121,6 +122,73 @@ __device__ float block_sum(float v, float *red) {
     return s;
 }
 
+// o-projection epilogue fused with the next RMSNorm: r = (sum of split partials) + residual,
+// stored bf16, then xn = RMSNorm(r) * gamma.  Same thread layout and arithmetic order as
+// splitk_reduce_kernel followed by rmsnorm_kernel, so the results are bit-identical to them.
+__global__ void __launch_bounds__(kNormThreads)
+    residual_rmsnorm_kernel(const float *__restrict__ part, int split, int M, int N,
+                                        const uint16_t *__restrict__ residual,
+                                        const uint16_t *__restrict__ gamma, float eps, uint16_t *r,
+                                        uint16_t *xn) {
+    __shared__ float red[32];
+    const int m = blockIdx.x;
+    const size_t plane = (size_t)M * N;
+    const float *pr = part + (size_t)m * N;
+    uint4 *rr = reinterpret_cast<uint4 *>(r + (size_t)m * N);
+    const int nv = N / 8;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        // slices summed in increasing order per element (as splitk_reduce_kernel), loaded as
+        // float4 pairs several slices ahead
+        const float4 *p4 = reinterpret_cast<const float4 *>(pr + 8 * i);
+        float4 lo = p4[0], hi = p4[1];
+#pragma unroll 4
+        for (int sl = 1; sl < split; ++sl) {
+            const float4 *q4 = reinterpret_cast<const float4 *>(pr + (size_t)sl * plane + 8 * i);
+            const float4 a = q4[0], b = q4[1];
+            lo.x = __fadd_rn(lo.x, a.x); lo.y = __fadd_rn(lo.y, a.y);
+            lo.z = __fadd_rn(lo.z, a.z); lo.w = __fadd_rn(lo.w, a.w);
+            hi.x = __fadd_rn(hi.x, b.x); hi.y = __fadd_rn(hi.y, b.y);
+            hi.z = __fadd_rn(hi.z, b.z); hi.w = __fadd_rn(hi.w, b.w);
+        }
+        float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        if (residual) {
+            const uint4 rw = ld_act_v4(residual + (size_t)m * N + 8 * i);
+            const uint32_t rs[4] = {rw.x, rw.y, rw.z, rw.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[2 * j] = __fadd_rn(v[2 * j], bf16_lo(rs[j]));
+                v[2 * j + 1] = __fadd_rn(v[2 * j + 1], bf16_hi(rs[j]));
+            }
+        }
+        const uint4 w = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                   pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+        rr[i] = w;
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = bf16_lo(ws[j]), b = bf16_hi(ws[j]);
+            ss = __fmaf_rn(a, a, ss);
+            ss = __fmaf_rn(b, b, ss);
+        }
+    }
+    const float tot = block_sum(ss, red);
+    const float inv = 1.0f / sqrtf(tot / (float)N + eps);
+    const uint4 *gr = reinterpret_cast<const uint4 *>(gamma);
+    uint4 *yr = reinterpret_cast<uint4 *>(xn + (size_t)m * N);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        const uint4 w = rr[i];
+        const uint4 gg = ld_act_v4(gr + i);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w}, gs[4] = {gg.x, gg.y, gg.z, gg.w};
+        uint32_t out[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            out[j] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16_lo(ws[j]), inv), bf16_lo(gs[j])),
+                                 __fmul_rn(__fmul_rn(bf16_hi(ws[j]), inv), bf16_hi(gs[j])));
+        yr[i] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+}
+
 // q/k/v/gate/beta epilogue: one CTA of d threads per (token, head).
 __global__ void qkvg_epilogue_kernel(const float *__restrict__ part, int split, int M, int H, int d,
                                      uint16_t *q, uint16_t *k, uint16_t *v, float *alpha,
@@ -150,7 +218,7 @@ __global__ void qkvg_epilogue_kernel(const float *__restrict__ part, int split, 
     if (i == 0) beta[(size_t)m * H + h] = 1.0f / (1.0f + expf(-sum(4 * Hd_ + h)));
 }
 
-__global__ void rmsnorm_kernel(int Hd, const uint16_t *__restrict__ x,
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(int Hd, const uint16_t *__restrict__ x,
                                const uint16_t *__restrict__ gamma, float eps, uint16_t *y) {
     __shared__ float red[32];
     const int m = blockIdx.x;
@@ -316,7 +384,7 @@ int run_splitk_reduce(const float *part, int split, int M, int N, const hla_bf16
 
 int run_rmsnorm(int M, int Hd, const hla_bf16 *x, const hla_bf16 *gamma, float eps, hla_bf16 *y,
                 cudaStream_t st) {
-    rmsnorm_kernel<<<M, 256, 0, st>>>(Hd, x, gamma, eps, y);
+    rmsnorm_kernel<<<M, kNormThreads, 0, st>>>(Hd, x, gamma, eps, y);
     return launch_status();
 }
 
@@ -446,4 +514,33 @@ extern "C" int hla_l2_prefetch(const void *ptr, size_t bytes, hla_stream stream)
     HLA_REQUIRE(bytes == 0 || aligned16(ptr), HLA_ERR_MISALIGNED);
     set_variant("l2_prefetch");
     return run_l2_prefetch(ptr, bytes, (cudaStream_t)stream);
+}
+
+extern "C" size_t skinny_proj_residual_rmsnorm_workspace_size(int M, int N, int K, int split) {
+    if (M < 1 || N < 8 || K < 32) return 0;
+    return (size_t)resolve_split(M, N, K, split) * M * N * sizeof(float);
+}
+
+extern "C" int skinny_proj_residual_rmsnorm(int M, int N, int K, const hla_bf16 *x,
+                                            const hla_bf16 *W, const hla_bf16 *residual,
+                                            const hla_bf16 *gamma, float eps, hla_bf16 *r,
+                                            hla_bf16 *xn, int split, void *ws, size_t ws_bytes,
+                                            hla_stream stream) {
+    HLA_REQUIRE(M >= 1 && N >= 8 && K >= 32 && split >= 0 && eps >= 0.f, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(M <= 256 && K % 32 == 0 && N % 8 == 0, HLA_ERR_UNSUPPORTED);
+    HLA_REQUIRE(x && W && gamma && r && xn, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(aligned16(x) && aligned16(W) && aligned16(gamma) && aligned16(r) && aligned16(xn) &&
+                    (!residual || aligned16(residual)),
+                HLA_ERR_MISALIGNED);
+    const size_t need = skinny_proj_residual_rmsnorm_workspace_size(M, N, K, split);
+    HLA_REQUIRE(ws && ws_bytes >= need, HLA_ERR_WORKSPACE);
+    HLA_REQUIRE(aligned16(ws), HLA_ERR_MISALIGNED);
+    const int s = resolve_split(M, N, K, split);
+    cudaStream_t st = (cudaStream_t)stream;
+    float *part = reinterpret_cast<float *>(ws);
+    int rc = run_dense(M, N, K, x, W, s, part, nullptr, 0, nullptr, st);
+    if (rc != HLA_OK) return rc;
+    residual_rmsnorm_kernel<<<M, kNormThreads, 0, st>>>(part, s, M, N, residual, gamma, eps, r, xn);
+    set_variant("proj_residual_rmsnorm<tt%d,split%d>", dense_tokens_per_tile(M), s);
+    return launch_status();
 }

@@ -1,7 +1,7 @@
 // One hybrid decode layer as a chain of the library's entry points, on one stream:
 //   x -> RMSNorm -> q/k/v/gate/beta projection (+ L2 norm, decay, write strength)
-//     -> KDA decode step (state in place) -> output projection + residual
-//     -> RMSNorm -> router -> routed + shared experts + residual -> y
+//     -> KDA decode step (state in place) -> output projection + residual + RMSNorm (one
+//     epilogue) -> router -> routed + shared experts + residual -> y
 // ("Hyper-optimizing Kimi K3 in vLLM", Part 1 secs. 1-4; "Kimi K3: From Day-0
 // Availability to Optimized Inference": residual adds and normalisation around the
 // projections).  The prefetch stream is passed to the MoE call, which warms the shared
@@ -37,7 +37,7 @@ LayerLayout layer_layout(const hla_layer *L, int M) {
         return p;
     };
     o.qkvg_bytes = kda_qkvg_proj_workspace_size(M, L->hidden, L->heads, L->dk, L->dv, 0);
-    o.oproj_bytes = skinny_proj_splitk_workspace_size(M, L->hidden, L->heads * L->dv, 0);
+    o.oproj_bytes = skinny_proj_residual_rmsnorm_workspace_size(M, L->hidden, L->heads * L->dv, 0);
     o.router_bytes = moe_route_topk_workspace_size(M, L->hidden, L->n_experts);
     o.moe_bytes = moe_expert_forward_workspace_size(M, L->hidden, L->inter, L->n_experts,
                                                    L->top_k, L->n_shared);
@@ -112,11 +112,10 @@ extern "C" int hla_decode_layer(const hla_layer *L, int M, const hla_bf16 *x, fl
     if ((r = kda_decode_step(M, H, d, d, S, state_idx, bf(lo.q), bf(lo.k), bf(lo.v), f32(lo.alpha),
                              f32(lo.beta), bf(lo.o), HLA_BF16, stream)) != HLA_OK)
         return r;
-    if ((r = skinny_proj_splitk(M, Hd, H * d, bf(lo.o), L->W_o, x, bf(lo.r), HLA_BF16, 0,
-                                lo.oproj_bytes ? w + lo.oproj_ws : nullptr, lo.oproj_bytes,
-                                stream)) != HLA_OK)
+    if ((r = skinny_proj_residual_rmsnorm(M, Hd, H * d, bf(lo.o), L->W_o, x, L->gamma_moe, L->eps,
+                                          bf(lo.r), bf(lo.x2), 0, w + lo.oproj_ws, lo.oproj_bytes,
+                                          stream)) != HLA_OK)
         return r;
-    if ((r = hla_rmsnorm(M, Hd, bf(lo.r), L->gamma_moe, L->eps, bf(lo.x2), stream)) != HLA_OK) return r;
     if ((r = moe_route_topk(M, Hd, L->n_experts, L->top_k, bf(lo.x2), L->W_router,
                             reinterpret_cast<int32_t *>(w + lo.idx), f32(lo.w), nullptr,
                             w + lo.router_ws, lo.router_bytes, stream)) != HLA_OK)

@@ -41,7 +41,7 @@ constexpr int kMoeThreads = 128;
 constexpr int kDispatchThreads = 1024;
 
 struct MoeLayout {
-    int M, Hd, I, E, k, nsh, P, U_max, KS, TT;
+    int M, Hd, I, E, k, nsh, P, U_max, KS, KSD, TT;
     bool shared_tc;      // shared experts on the tensor-core path instead of grouped work units
     int s_gu, s_dn;      // K slices of the shared experts' tensor-core products
     size_t off_meta, off_unit_expert, off_unit_off, off_item_gu, off_item_dn, off_pos_token,
@@ -49,7 +49,7 @@ struct MoeLayout {
 };
 
 struct MoeArgs {
-    int M, Hd, I, E, k, nsh, P, KS, TT;
+    int M, Hd, I, E, k, nsh, P, KS, KSD, TT;
     int nsh_units;  // shared experts run as grouped work units (0 when on the tensor-core path)
     const uint16_t *x;
     const int32_t *topk_idx;
@@ -63,6 +63,18 @@ struct MoeArgs {
 };
 
 int moe_tokens_per_tile(int M) { return M <= 8 ? 8 : 16; }
+
+// K slices of the down projection: only at the smallest batches, where the (units x 32-row
+// blocks) items alone leave each SM with a single wave of 128 KB items.
+int moe_down_split(int M, int Hd, int E, int k, int nsh) {
+    long units = (long)M * k < E ? (long)M * k : E;
+    units += nsh;
+    const long items = units * ((Hd + 31) / 32);
+    long s = (24L * sm_count() + items - 1) / items;
+    if (s < 1) s = 1;
+    if (s > 4) s = 4;
+    return (int)s;
+}
 
 int moe_gateup_split(int M, int I, int E, int k, int nsh) {
     const char *env = getenv("HLA_MOE_SPLIT");
@@ -85,6 +97,7 @@ MoeLayout moe_layout(int M, int Hd, int I, int E, int k, int nsh) {
     L.P = M * (k + nsh);
     L.U_max = E + nsh;
     L.KS = moe_gateup_split(M, I, E, k, nsh);
+    L.KSD = moe_down_split(M, Hd, E, k, nsh);
     L.TT = moe_tokens_per_tile(M);
     // Optional (HLA_SHARED_TC=1): past 16 tokens run each shared expert as a dense SwiGLU
     // over all M tokens on the tensor-core path instead of as a grouped work unit.  Off by
@@ -110,7 +123,7 @@ MoeLayout moe_layout(int M, int Hd, int I, int E, int k, int nsh) {
     L.off_h = take((size_t)L.P * I * sizeof(uint16_t));
     L.off_part_g = take(L.KS > 1 ? (size_t)L.KS * L.P * I * sizeof(float) : 0);
     L.off_part_u = take(L.KS > 1 ? (size_t)L.KS * L.P * I * sizeof(float) : 0);
-    L.off_ypart = take((size_t)L.P * Hd * sizeof(float));
+    L.off_ypart = take((size_t)L.KSD * L.P * Hd * sizeof(float));
     L.off_sh_g = take(L.shared_tc ? (size_t)L.s_gu * M * I * sizeof(float) : 0);
     L.off_sh_u = take(L.shared_tc ? (size_t)L.s_gu * M * I * sizeof(float) : 0);
     L.off_sh_d = take(L.shared_tc ? (size_t)L.s_dn * M * Hd * sizeof(float) : 0);
@@ -214,7 +227,7 @@ __global__ void __launch_bounds__(kDispatchThreads) moe_dispatch_kernel(const Mo
         const int n = a.unit_off[tid + 1] - a.unit_off[tid];
         const int ntg = (n + a.TT - 1) / a.TT;
         ig = nrb_gu * a.KS * ntg;
-        id = nrb_dn * ntg;
+        id = nrb_dn * ntg * a.KSD;
     }
     int tot_g, tot_d;
     const int og = block_exclusive_scan(ig, warp_tot, tot_g);
@@ -336,7 +349,8 @@ __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(const MoeArgs a) 
         const int p0 = a.unit_off[u], p1 = a.unit_off[u + 1];
         const int ntg = (p1 - p0 + a.TT - 1) / a.TT;
         const int tg = local % ntg;
-        const int rb = local / ntg;  // a block of 32 rows: two 16-row MMA tiles share the tokens
+        const int ks = (local / ntg) % a.KSD;
+        const int rb = local / ntg / a.KSD;  // a block of 32 rows: two 16-row MMA tiles share the tokens
         const int e = a.unit_expert[u];
         const uint16_t *Wd = (e < a.E ? a.W_down : a.Ws_down) +
                              (size_t)(e < a.E ? e : e - a.E) * a.Hd * a.I;
@@ -359,7 +373,9 @@ __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(const MoeArgs a) 
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) acc[h][nt][q] = 0.f;
-        warp_stream_tile<2, NT, 4>(wg, wg8, xr, 0, a.I, acc);
+        int kb, ke;
+        k_slice(a.I, a.KSD, ks, kb, ke);
+        warp_stream_tile<2, NT, 4>(wg, wg8, xr, kb, ke, acc);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -369,7 +385,7 @@ __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(const MoeArgs a) 
                     const int row = rbase + 16 * h + acc_row(q);
                     const int p = pt + acc_tok(nt, q);
                     if (row >= a.Hd || p >= p1) continue;
-                    a.ypart[(size_t)a.pos_slot[p] * a.Hd + row] = acc[h][nt][q];
+                    a.ypart[((size_t)ks * a.P + a.pos_slot[p]) * a.Hd + row] = acc[h][nt][q];
                 }
             }
         }
@@ -389,7 +405,15 @@ __global__ void moe_combine_kernel(const MoeArgs a) {
             if (e < 0 || e >= a.E) continue;
             w = a.topk_w[(size_t)m * a.k + j];
         }
-        const float4 v = reinterpret_cast<const float4 *>(a.ypart + ((size_t)m * S + j) * a.Hd)[c4];
+        const bool tc_slot = j >= a.k && a.nsh_units == 0;
+        const int nks = tc_slot ? 1 : a.KSD;
+        float4 v = reinterpret_cast<const float4 *>(a.ypart + ((size_t)m * S + j) * a.Hd)[c4];
+        for (int ks = 1; ks < nks; ++ks) {
+            const float4 t = reinterpret_cast<const float4 *>(
+                a.ypart + ((size_t)ks * a.P + (size_t)m * S + j) * a.Hd)[c4];
+            v.x = __fadd_rn(v.x, t.x); v.y = __fadd_rn(v.y, t.y);
+            v.z = __fadd_rn(v.z, t.z); v.w = __fadd_rn(v.w, t.w);
+        }
         acc.x = __fmaf_rn(w, v.x, acc.x);
         acc.y = __fmaf_rn(w, v.y, acc.y);
         acc.z = __fmaf_rn(w, v.z, acc.z);
@@ -470,6 +494,7 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     char *w = reinterpret_cast<char *>(ws);
     MoeArgs a;
     a.M = M; a.Hd = Hd; a.I = I; a.E = E; a.k = k; a.nsh = nsh; a.P = L.P; a.KS = L.KS; a.TT = L.TT;
+    a.KSD = L.KSD;
     a.nsh_units = L.shared_tc ? 0 : nsh;
     a.x = x; a.topk_idx = topk_idx; a.topk_w = topk_w;
     a.W_gate = W_gate; a.W_up = W_up; a.W_down = W_down;
@@ -563,7 +588,8 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     moe_combine_kernel<<<cgrid, 128, 0, st>>>(a);
     if ((r = launch_status()) != HLA_OK) return r;
     if (side && cudaStreamWaitEvent(st, g_moe_events.join, 0) != cudaSuccess) return HLA_ERR_CUDA;
-    set_variant("moe<tt%d,ks%d%s%s>", L.TT, L.KS, L.shared_tc ? ",shared_tc" : "", side ? ",prefetch" : "");
+    set_variant("moe<tt%d,ks%d,ksd%d%s%s>", L.TT, L.KS, L.KSD, L.shared_tc ? ",shared_tc" : "",
+                side ? ",prefetch" : "");
     return HLA_OK;
 }
 

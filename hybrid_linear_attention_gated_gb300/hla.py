@@ -51,6 +51,9 @@ SIGNATURES = {
     "kda_spec_replay_verify": (c_int, [c_int] * 6 + [P] * 14 + [c_int, P]),
     "skinny_proj_splitk_workspace_size": (c_size_t, [c_int] * 4),
     "skinny_proj_splitk": (c_int, [c_int] * 3 + [P] * 4 + [c_int, c_int, P, c_size_t, P]),
+    "skinny_proj_residual_rmsnorm_workspace_size": (c_size_t, [c_int] * 4),
+    "skinny_proj_residual_rmsnorm": (c_int, [c_int] * 3 + [P] * 4 + [c_float, P, P, c_int, P,
+                                                                      c_size_t, P]),
     "kda_qkvg_proj_workspace_size": (c_size_t, [c_int] * 6),
     "kda_qkvg_proj": (c_int, [c_int] * 5 + [P] * 7 + [c_int, P, c_size_t, P]),
     "hla_rmsnorm": (c_int, [c_int, c_int, P, P, c_float, P, P]),
@@ -167,6 +170,17 @@ def skinny_proj_splitk_workspace_size(M, N, K, split=0):
 def skinny_proj_splitk(M, N, K, x, W, residual, y, y_dtype, split, ws, ws_bytes, stream=None):
     return _check("skinny_proj_splitk", load().skinny_proj_splitk(
         M, N, K, _p(x), _p(W), _p(residual), _p(y), y_dtype, split, _p(ws), ws_bytes,
+        _stream(stream)))
+
+
+def skinny_proj_residual_rmsnorm_workspace_size(M, N, K, split=0):
+    return load().skinny_proj_residual_rmsnorm_workspace_size(M, N, K, split)
+
+
+def skinny_proj_residual_rmsnorm(M, N, K, x, W, residual, gamma, eps, r, xn, split, ws, ws_bytes,
+                                 stream=None):
+    return _check("skinny_proj_residual_rmsnorm", load().skinny_proj_residual_rmsnorm(
+        M, N, K, _p(x), _p(W), _p(residual), _p(gamma), eps, _p(r), _p(xn), split, _p(ws), ws_bytes,
         _stream(stream)))
 
 

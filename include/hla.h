@@ -179,6 +179,23 @@ int skinny_proj_splitk(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W
                        void *ws, size_t ws_bytes, hla_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * Output projection + residual + the following RMSNorm in one pass over the result.
+ * [KIMI-WEBINAR] fusing the residual addition and normalisation into the projection;
+ * [VLLM-K3] Part 1 sec. 2 (the single-GPU part: projection, then the attention residual).
+ *  r  = residual + x W^T            stored bf16 [M, N]   (residual bf16 [M, N] or NULL)
+ *  xn = r * gamma / sqrt(mean(r^2) + eps)   over each row, stored bf16 [M, N]
+ *  x bf16 [M, K]; W bf16 [N, K]; gamma bf16 [N]; K % 32 == 0, N % 8 == 0, 1 <= M <= 256.
+ *  split as skinny_proj_splitk (0 = automatic).  Bit-identical to skinny_proj_splitk (bf16
+ *  output) followed by hla_rmsnorm with the same split.  The workspace holds the fp32
+ *  split partials (at least one slice).
+ * -------------------------------------------------------------------------*/
+size_t skinny_proj_residual_rmsnorm_workspace_size(int M, int N, int K, int split);
+int skinny_proj_residual_rmsnorm(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W,
+                                 const hla_bf16 *residual, const hla_bf16 *gamma, float eps,
+                                 hla_bf16 *r, hla_bf16 *xn, int split, void *ws, size_t ws_bytes,
+                                 hla_stream stream);
+
+/* ---------------------------------------------------------------------------
  * KDA input projection with its epilogue (decode layer).  [VLLM-K3] Part 1
  * sec. 1 (attention input projections) feeding the KDA decode kernel.
  *  z = x W^T, W bf16 [(3*dk + dv)*H + H, Hd] with row blocks

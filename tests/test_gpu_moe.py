@@ -63,6 +63,33 @@ def test_skinny_proj(dev, M, N, K, split, res, out):
     assert frob_rel(f64(y), ref) < tol
 
 
+@pytest.mark.parametrize("M", [1, 8, 64])
+def test_proj_residual_rmsnorm(dev, M):
+    """o-projection + residual + RMSNorm in one epilogue: bit-identical to skinny_proj_splitk
+    followed by hla_rmsnorm (same split), and within tolerance of the oracle."""
+    N, K = 7168, 4096
+    g = inputs.generator(90 + M)
+    x, W = inputs.activations(M, K, g).to(dev), inputs.weight((N, K), g).to(dev)
+    res, gam = inputs.activations(M, N, g).to(dev), inputs.gains(N, g).to(dev)
+    r1 = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    xn1 = torch.empty_like(r1)
+    nb = hla.skinny_proj_residual_rmsnorm_workspace_size(M, N, K, 0)
+    ws = _ws(nb, dev)
+    hla.skinny_proj_residual_rmsnorm(M, N, K, x, W, res, gam, 1e-6, r1, xn1, 0, ws, nb)
+    split = int(hla.hla_last_variant().split("split")[1].rstrip(">"))
+    r2 = torch.empty_like(r1)
+    xn2 = torch.empty_like(r1)
+    ws2 = _ws(hla.skinny_proj_splitk_workspace_size(M, N, K, split), dev)
+    hla.skinny_proj_splitk(M, N, K, x, W, res, r2, hla.HLA_BF16, split, ws2, ws2.numel())
+    hla.hla_rmsnorm(M, N, r2, gam, 1e-6, xn2)
+    torch.cuda.synchronize()
+    assert torch.equal(r1, r2) and torch.equal(xn1, xn2)
+    r_ref = oracle.moe.linear(f64(x), f64(W)) + f64(res)
+    assert frob_rel(f64(r1), r_ref) < PROJ_FROB_REL_BF16
+    xn_ref = oracle.moe.rmsnorm(oracle.numerics.round_bf16(r_ref), f64(gam), 1e-6)
+    assert frob_rel(f64(xn1), xn_ref) < PROJ_FROB_REL_BF16
+
+
 def test_split_counts_agree(dev):
     M, N, K = 4, 512, 2048
     g = inputs.generator(3)
