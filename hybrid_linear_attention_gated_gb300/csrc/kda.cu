@@ -58,8 +58,10 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
     constexpr int NTHR = kRowGroups * CG;
     constexpr int TMAX = MODE == kDecode ? 1 : (MODE == kReplayVerify ? 2 * kMaxWindow : kMaxWindow);
     constexpr bool WRITE_O = MODE != kReplay;
+    static_assert(TMAX <= NTHR, "one thread per token loads beta");
 
-    __shared__ float sq[TMAX][DK], sk[TMAX][DK], sa[TMAX][DK], sv[TMAX][CW], sb[TMAX];
+    __shared__ __align__(16) float sq[TMAX][DK], sk[TMAX][DK], sa[TMAX][DK], sv[TMAX][CW];
+    __shared__ float sb[TMAX];
     __shared__ float4 red_u[2][kRowGroups][CG], red_w[2][kRowGroups][CG];
     __shared__ float red_qk[2][kRowGroups];
 
@@ -94,22 +96,79 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
     for (int j = 0; j < RPT; ++j)
         s[j] = *reinterpret_cast<const float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV);
 
-    // per-token vectors: token t of sequence b is row (b*T + t) of its [B, T, H, .] tensor
+    // per-token vectors: token t of sequence b is row (b*T + t) of its [B, T, H, .] tensor.
+    // Two loaders fill the same shared arrays with the same values (so results do not depend
+    // on the choice); which one is faster depends on the CTA width and the program length.
     const int Tld = MODE == kDecode ? 1 : p.T;
-    for (int t = 0; t < steps; ++t) {
-        const bool pre = t < n_pre;
-        const uint16_t *q = pre ? p.qp : p.q, *k = pre ? p.kp : p.k, *v = pre ? p.vp : p.v;
-        const float *al = pre ? p.alphap : p.alpha, *be = pre ? p.betap : p.beta;
-        const size_t tok = pre ? ((size_t)b * p.Tp + t) * p.H + h
-                               : ((size_t)b * Tld + (t - n_pre)) * p.H + h;
-        for (int i = tid; i < DK; i += NTHR) {
-            sq[t][i] = bf16_bits_to_float(q[tok * DK + i]);
-            sk[t][i] = bf16_bits_to_float(k[tok * DK + i]);
-            sa[t][i] = al[tok * DK + i];
-        }
-        for (int c = tid; c < CW; c += NTHR) sv[t][c] = bf16_bits_to_float(v[tok * DV + col0 + c]);
-        if (tid == 0) sb[t] = be[tok];
+    // beta first, into a register, so its load overlaps the vector loads below
+    float beta_r = 0.f;
+    if (tid < steps) {
+        const bool pre = tid < n_pre;
+        const size_t tok = pre ? ((size_t)b * p.Tp + tid) * p.H + h
+                               : ((size_t)b * Tld + (tid - n_pre)) * p.H + h;
+        beta_r = (pre ? p.betap : p.beta)[tok];
     }
+    constexpr bool kVectorLoads = CW <= 32 || MODE == kReplayVerify;
+    if constexpr (kVectorLoads) {
+        // Work list: per token DK/8 chunks of q, DK/8 of k, DK/4 of alpha and CW/8 of v, each
+        // one 128-bit load; each thread issues LDEPTH loads before storing any of them, so its
+        // loads overlap instead of waiting one latency each (narrow CTAs, long programs).
+        constexpr int QC = DK / 8, AC = DK / 4, VC = CW / 8, PER_TOK = 2 * QC + AC + VC;
+        constexpr int LDEPTH = 4;
+        const int n_items = steps * PER_TOK;
+        for (int x0 = tid; x0 < n_items; x0 += LDEPTH * NTHR) {
+            uint4 r[LDEPTH];
+#pragma unroll
+            for (int u = 0; u < LDEPTH; ++u) {
+                const int x = x0 + u * NTHR;
+                if (x >= n_items) break;
+                const int t = x / PER_TOK, c = x - t * PER_TOK;
+                const bool pre = t < n_pre;
+                const size_t tok = pre ? ((size_t)b * p.Tp + t) * p.H + h
+                                       : ((size_t)b * Tld + (t - n_pre)) * p.H + h;
+                const void *src;
+                if (c < QC) src = (pre ? p.qp : p.q) + tok * DK + 8 * c;
+                else if (c < 2 * QC) src = (pre ? p.kp : p.k) + tok * DK + 8 * (c - QC);
+                else if (c < 2 * QC + AC) src = (pre ? p.alphap : p.alpha) + tok * DK + 4 * (c - 2 * QC);
+                else src = (pre ? p.vp : p.v) + tok * DV + col0 + 8 * (c - 2 * QC - AC);
+                r[u] = ld_act_v4(src);
+            }
+#pragma unroll
+            for (int u = 0; u < LDEPTH; ++u) {
+                const int x = x0 + u * NTHR;
+                if (x >= n_items) break;
+                const int t = x / PER_TOK, c = x - t * PER_TOK;
+                const uint4 w = r[u];
+                if (c < 2 * QC + AC && c >= 2 * QC) {
+                    *reinterpret_cast<uint4 *>(&sa[t][4 * (c - 2 * QC)]) = w;  // fp32 bits as loaded
+                    continue;
+                }
+                float *dst = c < QC ? &sq[t][8 * c]
+                           : c < 2 * QC ? &sk[t][8 * (c - QC)] : &sv[t][8 * (c - 2 * QC - AC)];
+                reinterpret_cast<float4 *>(dst)[0] =
+                    make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+                reinterpret_cast<float4 *>(dst)[1] =
+                    make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+            }
+        }
+    } else {
+        // scalar loads, one unrolled pass per token (measured faster for 64/128-column
+        // slices in the decode, verify and replay programs)
+        for (int t = 0; t < steps; ++t) {
+            const bool pre = t < n_pre;
+            const uint16_t *q = pre ? p.qp : p.q, *k = pre ? p.kp : p.k, *v = pre ? p.vp : p.v;
+            const float *al = pre ? p.alphap : p.alpha;
+            const size_t tok = pre ? ((size_t)b * p.Tp + t) * p.H + h
+                                   : ((size_t)b * Tld + (t - n_pre)) * p.H + h;
+            for (int i = tid; i < DK; i += NTHR) {
+                sq[t][i] = bf16_bits_to_float(q[tok * DK + i]);
+                sk[t][i] = bf16_bits_to_float(k[tok * DK + i]);
+                sa[t][i] = al[tok * DK + i];
+            }
+            for (int c = tid; c < CW; c += NTHR) sv[t][c] = bf16_bits_to_float(v[tok * DV + col0 + c]);
+        }
+    }
+    if (tid < steps) sb[tid] = beta_r;  // steps <= 2 * kMaxWindow <= NTHR
     __syncthreads();
 
     for (int t = 0; t < steps; ++t) {
