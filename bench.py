@@ -338,6 +338,39 @@ def moe_sweep(torch, hla, inputs, wl, dev, peak):
     return res
 
 
+def extend_sweep(torch, hla, inputs, dev, peak):
+    """Mixed batches through kda_extend: decoding sequences (1 token) next to prefill chunks,
+    states in a rotating pool larger than L2.  Tokens of one sequence are applied in order
+    (the recurrent form), so a long chunk is a serial chain."""
+    c = CFG
+    H, d = c["H"], c["d"]
+    tok_bytes = 3 * d * 2 + d * 4 + 4 + 4 * d
+    pool_slots = 512 * 2 ** 20 // (H * d * d * 4)
+    pool = torch.randn(pool_slots, H, d, d, device=dev).mul_(0.05)
+    res = []
+    for name, lens in (("64 decode", [1] * 64), ("60 decode + 4 x 32-token chunks", [1] * 60 + [32] * 4),
+                       ("60 decode + 4 x 128-token chunks", [1] * 60 + [128] * 4),
+                       ("4 x 512-token chunks", [512] * 4)):
+        B = len(lens)
+        cu = torch.tensor([0] + list(__import__("itertools").accumulate(lens)), dtype=torch.int32, device=dev)
+        N = int(cu[-1])
+        u = inputs.kda_inputs((N,), H, d, d, inputs.generator(7800 + N, dev), dev)
+        o = torch.empty(N, H, d, device=dev)
+        iters = max(4, min(32, pool_slots // B))
+        idxs = [torch.arange(i * B, (i + 1) * B, dtype=torch.int32, device=dev) % pool_slots
+                for i in range(iters)]
+
+        def fn(i, B=B, cu=cu, u=u, o=o, idxs=idxs):
+            hla.kda_extend(B, cu, H, d, d, pool, idxs[i % len(idxs)], u["q"], u["k"], u["v"],
+                           u["alpha"], u["beta"], o)
+        t = graph_time(torch, fn, iters)
+        nbytes = B * H * 8 * d * d + N * H * tok_bytes
+        res.append(dict(batch=name, tokens=N, us=round(t * 1e6, 2), tokens_per_s=round(N / t),
+                        gbs=round(nbytes / t / 1e9, 1), frac=round(nbytes / t / 1e9 / peak, 3)))
+    del pool
+    return res
+
+
 def spec_sweep(torch, hla, inputs, wl, dev, peak):
     """Speculative window, T=4, accepted length uniform in 0..4, at B=16 (33.5 MB of committed
     state: fits in L2) and B=64 (134 MB: does not), two forms per step: separate (verify +
@@ -550,6 +583,7 @@ def run_ours(args):
         sweeps["moe"] = moe_sweep(torch, hla, inputs, wl, dev, peak)
         sweeps["layer"] = layer_sweep(torch, hla, inputs, wl, dev, peak)
         sweeps["spec_window"] = spec_sweep(torch, hla, inputs, wl, dev, peak)
+        sweeps["kda_extend"] = extend_sweep(torch, hla, inputs, dev, peak)
     clocks = sampler.stop()
 
     if rank != 0:

@@ -28,16 +28,17 @@ namespace {
 constexpr int kRowGroups = 8;
 constexpr int kMaxWindow = 8;
 
-enum KdaMode { kDecode = 0, kVerify = 1, kReplay = 2, kReplayVerify = 3 };
+enum KdaMode { kDecode = 0, kVerify = 1, kReplay = 2, kReplayVerify = 3, kExtend = 4 };
 
 struct KdaParams {
     float *S;
     const int32_t *state_idx;
-    const uint16_t *q, *k, *v;          // this call's tokens [B, T, H, .] (T = 1 for decode)
-    const float *alpha, *beta;
+    const uint16_t *q, *k, *v;          // this call's tokens [B, T, H, .] (T = 1 for decode);
+    const float *alpha, *beta;          //   extend: packed [N, H, .] rows cu_seqlens[b]..[b+1]-1
     const uint16_t *qp, *kp, *vp;       // replay-verify: the previous window [B, Tp, H, .]
     const float *alphap, *betap;
     const int32_t *accepted;            // replay: of this window; replay-verify: of the previous one
+    const int32_t *cu_seqlens;          // extend: [B + 1] token offsets of the sequences
     void *o;
     int o_bf16;
     int B, T, Tp, H;
@@ -45,9 +46,11 @@ struct KdaParams {
 
 // Each CTA runs a short program over its (sequence, head, column slice):
 //   n_pre steps from the previous window, then commit the state (replay-verify only);
-//   n_main steps from this call's tokens, writing o (decode, verify, replay-verify) and/or
-//   committing the state at the end (decode, replay).
-// Every step is the same arithmetic, so any combination is bit-identical to the separate calls.
+//   n_main steps from this call's tokens, writing o (decode, verify, replay-verify, extend)
+//   and/or committing the state at the end (decode, replay, extend).
+// Tokens are staged through shared memory in blocks of TMAX; the state stays in registers
+// for the whole program.  Every step is the same arithmetic, so any combination is
+// bit-identical to the corresponding sequence of single steps.
 template <int DK, int CW, int MODE>
 __global__ void __launch_bounds__(kRowGroups *CW / 4)
     kda_recur_kernel(const KdaParams p) {
@@ -58,6 +61,7 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
     constexpr int NTHR = kRowGroups * CG;
     constexpr int TMAX = MODE == kDecode ? 1 : (MODE == kReplayVerify ? 2 * kMaxWindow : kMaxWindow);
     constexpr bool WRITE_O = MODE != kReplay;
+    constexpr bool COMMIT_END = MODE == kDecode || MODE == kReplay || MODE == kExtend;
     static_assert(TMAX <= NTHR, "one thread per token loads beta");
 
     __shared__ __align__(16) float sq[TMAX][DK], sk[TMAX][DK], sa[TMAX][DK], sv[TMAX][CW];
@@ -75,6 +79,7 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
     const int col0 = slice * CW;
 
     int n_pre = 0, n_main = MODE == kDecode ? 1 : p.T;
+    int seq0 = 0;
     if (MODE == kReplay || MODE == kReplayVerify) {
         const int lim = MODE == kReplay ? p.T : p.Tp;
         const int a0 = p.accepted[b];
@@ -86,7 +91,21 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
             n_pre = a;
         }
     }
+    if (MODE == kExtend) {
+        seq0 = p.cu_seqlens[b];
+        n_main = p.cu_seqlens[b + 1] - seq0;
+        if (n_main <= 0) return;  // no new tokens: the state is not touched
+    }
     const int steps = n_pre + n_main;
+    const int Tld = MODE == kDecode ? 1 : p.T;
+
+    // row of step t in its [., H, .] token tensor (previous window, this window, or packed)
+    auto token_row = [&](int t) -> size_t {
+        if (t < n_pre) return ((size_t)b * p.Tp + t) * p.H + h;
+        const int tm = t - n_pre;
+        if (MODE == kExtend) return ((size_t)seq0 + tm) * p.H + h;
+        return ((size_t)b * Tld + tm) * p.H + h;
+    };
 
     const int slot = p.state_idx ? p.state_idx[b] : b;
     float *Sb = p.S + ((size_t)slot * p.H + h) * (size_t)(DK * DV) + col0 + cg * 4;
@@ -96,156 +115,161 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
     for (int j = 0; j < RPT; ++j)
         s[j] = *reinterpret_cast<const float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV);
 
-    // per-token vectors: token t of sequence b is row (b*T + t) of its [B, T, H, .] tensor.
-    // Two loaders fill the same shared arrays with the same values (so results do not depend
-    // on the choice); which one is faster depends on the CTA width and the program length.
-    const int Tld = MODE == kDecode ? 1 : p.T;
-    // beta first, into a register, so its load overlaps the vector loads below
-    float beta_r = 0.f;
-    if (tid < steps) {
-        const bool pre = tid < n_pre;
-        const size_t tok = pre ? ((size_t)b * p.Tp + tid) * p.H + h
-                               : ((size_t)b * Tld + (tid - n_pre)) * p.H + h;
-        beta_r = (pre ? p.betap : p.beta)[tok];
-    }
-    constexpr bool kVectorLoads = CW <= 32 || MODE == kReplayVerify;
-    if constexpr (kVectorLoads) {
-        // Work list: per token DK/8 chunks of q, DK/8 of k, DK/4 of alpha and CW/8 of v, each
-        // one 128-bit load; each thread issues LDEPTH loads before storing any of them, so its
-        // loads overlap instead of waiting one latency each (narrow CTAs, long programs).
-        constexpr int QC = DK / 8, AC = DK / 4, VC = CW / 8, PER_TOK = 2 * QC + AC + VC;
-        constexpr int LDEPTH = 4;
-        const int n_items = steps * PER_TOK;
-        for (int x0 = tid; x0 < n_items; x0 += LDEPTH * NTHR) {
-            uint4 r[LDEPTH];
-#pragma unroll
-            for (int u = 0; u < LDEPTH; ++u) {
-                const int x = x0 + u * NTHR;
-                if (x >= n_items) break;
-                const int t = x / PER_TOK, c = x - t * PER_TOK;
-                const bool pre = t < n_pre;
-                const size_t tok = pre ? ((size_t)b * p.Tp + t) * p.H + h
-                                       : ((size_t)b * Tld + (t - n_pre)) * p.H + h;
-                const void *src;
-                if (c < QC) src = (pre ? p.qp : p.q) + tok * DK + 8 * c;
-                else if (c < 2 * QC) src = (pre ? p.kp : p.k) + tok * DK + 8 * (c - QC);
-                else if (c < 2 * QC + AC) src = (pre ? p.alphap : p.alpha) + tok * DK + 4 * (c - 2 * QC);
-                else src = (pre ? p.vp : p.v) + tok * DV + col0 + 8 * (c - 2 * QC - AC);
-                r[u] = ld_act_v4(src);
-            }
-#pragma unroll
-            for (int u = 0; u < LDEPTH; ++u) {
-                const int x = x0 + u * NTHR;
-                if (x >= n_items) break;
-                const int t = x / PER_TOK, c = x - t * PER_TOK;
-                const uint4 w = r[u];
-                if (c < 2 * QC + AC && c >= 2 * QC) {
-                    *reinterpret_cast<uint4 *>(&sa[t][4 * (c - 2 * QC)]) = w;  // fp32 bits as loaded
-                    continue;
-                }
-                float *dst = c < QC ? &sq[t][8 * c]
-                           : c < 2 * QC ? &sk[t][8 * (c - QC)] : &sv[t][8 * (c - 2 * QC - AC)];
-                reinterpret_cast<float4 *>(dst)[0] =
-                    make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
-                reinterpret_cast<float4 *>(dst)[1] =
-                    make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
-            }
-        }
-    } else {
-        // scalar loads, one unrolled pass per token (measured faster for 64/128-column
-        // slices in the decode, verify and replay programs)
-        for (int t = 0; t < steps; ++t) {
-            const bool pre = t < n_pre;
-            const uint16_t *q = pre ? p.qp : p.q, *k = pre ? p.kp : p.k, *v = pre ? p.vp : p.v;
-            const float *al = pre ? p.alphap : p.alpha;
-            const size_t tok = pre ? ((size_t)b * p.Tp + t) * p.H + h
-                                   : ((size_t)b * Tld + (t - n_pre)) * p.H + h;
-            for (int i = tid; i < DK; i += NTHR) {
-                sq[t][i] = bf16_bits_to_float(q[tok * DK + i]);
-                sk[t][i] = bf16_bits_to_float(k[tok * DK + i]);
-                sa[t][i] = al[tok * DK + i];
-            }
-            for (int c = tid; c < CW; c += NTHR) sv[t][c] = bf16_bits_to_float(v[tok * DV + col0 + c]);
-        }
-    }
-    if (tid < steps) sb[tid] = beta_r;  // steps <= 2 * kMaxWindow <= NTHR
-    __syncthreads();
+    // Only extend programs can exceed one block of TMAX tokens; for the others the loop body
+    // runs once with every step in it (and compiles to straight-line code).
+    constexpr bool BLOCKED = MODE == kExtend;
+    for (int t0 = 0; BLOCKED ? t0 < steps : t0 == 0; t0 += TMAX) {
+        const int tn = !BLOCKED ? steps : (steps - t0 < TMAX ? steps - t0 : TMAX);
+        if (BLOCKED && t0 > 0) __syncthreads();  // the previous block's tokens are no longer read
 
-    for (int t = 0; t < steps; ++t) {
-        const int buf = t & 1;
-        float4 pu = make_float4(0.f, 0.f, 0.f, 0.f), pw = pu;
-        float pqk = 0.f;
-#pragma unroll
-        for (int j = 0; j < RPT; ++j) {
-            const int i = rg + kRowGroups * j;
-            const float a = sa[t][i], kk = sk[t][i], qq = sq[t][i];
-            s[j].x = __fmul_rn(s[j].x, a);
-            s[j].y = __fmul_rn(s[j].y, a);
-            s[j].z = __fmul_rn(s[j].z, a);
-            s[j].w = __fmul_rn(s[j].w, a);
-            pu.x = __fmaf_rn(kk, s[j].x, pu.x);
-            pu.y = __fmaf_rn(kk, s[j].y, pu.y);
-            pu.z = __fmaf_rn(kk, s[j].z, pu.z);
-            pu.w = __fmaf_rn(kk, s[j].w, pu.w);
-            pw.x = __fmaf_rn(qq, s[j].x, pw.x);
-            pw.y = __fmaf_rn(qq, s[j].y, pw.y);
-            pw.z = __fmaf_rn(qq, s[j].z, pw.z);
-            pw.w = __fmaf_rn(qq, s[j].w, pw.w);
-            pqk = __fmaf_rn(qq, kk, pqk);
+        // Token vectors of steps t0 .. t0+tn-1 into slots 0..tn-1.  Two loaders fill the same
+        // shared arrays with the same values (results do not depend on the choice); which is
+        // faster depends on the CTA width and the program length.  beta goes to a register
+        // first so its load overlaps the others.
+        float beta_r = 0.f;
+        if (tid < tn) {
+            const int t = t0 + tid;
+            beta_r = (t < n_pre ? p.betap : p.beta)[token_row(t)];
         }
-        red_u[buf][rg][cg] = pu;
-        red_w[buf][rg][cg] = pw;
-        if (cg == 0) red_qk[buf][rg] = pqk;
+        constexpr bool kVectorLoads = CW <= 32 || MODE == kReplayVerify || MODE == kExtend;
+        if constexpr (kVectorLoads) {
+            // per token DK/8 chunks of q, DK/8 of k, DK/4 of alpha and CW/8 of v, one 128-bit
+            // load each; a thread issues LDEPTH loads before storing any of them
+            constexpr int QC = DK / 8, AC = DK / 4, VC = CW / 8, PER_TOK = 2 * QC + AC + VC;
+            constexpr int LDEPTH = 4;
+            const int n_items = tn * PER_TOK;
+            for (int x0 = tid; x0 < n_items; x0 += LDEPTH * NTHR) {
+                uint4 r[LDEPTH];
+#pragma unroll
+                for (int u = 0; u < LDEPTH; ++u) {
+                    const int x = x0 + u * NTHR;
+                    if (x >= n_items) break;
+                    const int tt = x / PER_TOK, c = x - tt * PER_TOK;
+                    const int t = t0 + tt;
+                    const bool pre = t < n_pre;
+                    const size_t tok = token_row(t);
+                    const void *src;
+                    if (c < QC) src = (pre ? p.qp : p.q) + tok * DK + 8 * c;
+                    else if (c < 2 * QC) src = (pre ? p.kp : p.k) + tok * DK + 8 * (c - QC);
+                    else if (c < 2 * QC + AC) src = (pre ? p.alphap : p.alpha) + tok * DK + 4 * (c - 2 * QC);
+                    else src = (pre ? p.vp : p.v) + tok * DV + col0 + 8 * (c - 2 * QC - AC);
+                    r[u] = ld_act_v4(src);
+                }
+#pragma unroll
+                for (int u = 0; u < LDEPTH; ++u) {
+                    const int x = x0 + u * NTHR;
+                    if (x >= n_items) break;
+                    const int tt = x / PER_TOK, c = x - tt * PER_TOK;
+                    const uint4 w = r[u];
+                    if (c < 2 * QC + AC && c >= 2 * QC) {
+                        *reinterpret_cast<uint4 *>(&sa[tt][4 * (c - 2 * QC)]) = w;  // fp32 bits
+                        continue;
+                    }
+                    float *dst = c < QC ? &sq[tt][8 * c]
+                               : c < 2 * QC ? &sk[tt][8 * (c - QC)] : &sv[tt][8 * (c - 2 * QC - AC)];
+                    reinterpret_cast<float4 *>(dst)[0] =
+                        make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+                    reinterpret_cast<float4 *>(dst)[1] =
+                        make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+                }
+            }
+        } else {
+            // scalar loads, one unrolled pass per token (measured faster for 64/128-column
+            // slices in the decode, verify and replay programs)
+            for (int tt = 0; tt < tn; ++tt) {
+                const int t = t0 + tt;
+                const bool pre = t < n_pre;
+                const uint16_t *q = pre ? p.qp : p.q, *k = pre ? p.kp : p.k, *v = pre ? p.vp : p.v;
+                const float *al = pre ? p.alphap : p.alpha;
+                const size_t tok = token_row(t);
+                for (int i = tid; i < DK; i += NTHR) {
+                    sq[tt][i] = bf16_bits_to_float(q[tok * DK + i]);
+                    sk[tt][i] = bf16_bits_to_float(k[tok * DK + i]);
+                    sa[tt][i] = al[tok * DK + i];
+                }
+                for (int c = tid; c < CW; c += NTHR) sv[tt][c] = bf16_bits_to_float(v[tok * DV + col0 + c]);
+            }
+        }
+        if (tid < tn) sb[tid] = beta_r;
         __syncthreads();
 
-        float4 u = red_u[buf][0][cg], w = red_w[buf][0][cg];
-        float qk = red_qk[buf][0];
+        for (int tt = 0; tt < tn; ++tt) {
+            const int t = t0 + tt;
+            const int buf = t & 1;
+            float4 pu = make_float4(0.f, 0.f, 0.f, 0.f), pw = pu;
+            float pqk = 0.f;
 #pragma unroll
-        for (int r = 1; r < kRowGroups; ++r) {
-            const float4 ur = red_u[buf][r][cg], wr = red_w[buf][r][cg];
-            u.x = __fadd_rn(u.x, ur.x); u.y = __fadd_rn(u.y, ur.y);
-            u.z = __fadd_rn(u.z, ur.z); u.w = __fadd_rn(u.w, ur.w);
-            w.x = __fadd_rn(w.x, wr.x); w.y = __fadd_rn(w.y, wr.y);
-            w.z = __fadd_rn(w.z, wr.z); w.w = __fadd_rn(w.w, wr.w);
-            qk = __fadd_rn(qk, red_qk[buf][r]);
-        }
-        const float bt = sb[t];
-        float4 d;
-        d.x = __fmul_rn(bt, __fsub_rn(sv[t][cg * 4 + 0], u.x));
-        d.y = __fmul_rn(bt, __fsub_rn(sv[t][cg * 4 + 1], u.y));
-        d.z = __fmul_rn(bt, __fsub_rn(sv[t][cg * 4 + 2], u.z));
-        d.w = __fmul_rn(bt, __fsub_rn(sv[t][cg * 4 + 3], u.w));
-#pragma unroll
-        for (int j = 0; j < RPT; ++j) {
-            const float kk = sk[t][rg + kRowGroups * j];
-            s[j].x = __fmaf_rn(kk, d.x, s[j].x);
-            s[j].y = __fmaf_rn(kk, d.y, s[j].y);
-            s[j].z = __fmaf_rn(kk, d.z, s[j].z);
-            s[j].w = __fmaf_rn(kk, d.w, s[j].w);
-        }
-        if (WRITE_O && t >= n_pre && rg == 0) {
-            float4 o;
-            o.x = __fmaf_rn(qk, d.x, w.x);
-            o.y = __fmaf_rn(qk, d.y, w.y);
-            o.z = __fmaf_rn(qk, d.z, w.z);
-            o.w = __fmaf_rn(qk, d.w, w.w);
-            const size_t oo = (((size_t)b * Tld + (t - n_pre)) * p.H + h) * DV + col0 + cg * 4;
-            if (p.o_bf16) {
-                uint2 pk = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
-                *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.o) + oo) = pk;
-            } else {
-                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + oo) = o;
+            for (int j = 0; j < RPT; ++j) {
+                const int i = rg + kRowGroups * j;
+                const float a = sa[tt][i], kk = sk[tt][i], qq = sq[tt][i];
+                s[j].x = __fmul_rn(s[j].x, a);
+                s[j].y = __fmul_rn(s[j].y, a);
+                s[j].z = __fmul_rn(s[j].z, a);
+                s[j].w = __fmul_rn(s[j].w, a);
+                pu.x = __fmaf_rn(kk, s[j].x, pu.x);
+                pu.y = __fmaf_rn(kk, s[j].y, pu.y);
+                pu.z = __fmaf_rn(kk, s[j].z, pu.z);
+                pu.w = __fmaf_rn(kk, s[j].w, pu.w);
+                pw.x = __fmaf_rn(qq, s[j].x, pw.x);
+                pw.y = __fmaf_rn(qq, s[j].y, pw.y);
+                pw.z = __fmaf_rn(qq, s[j].z, pw.z);
+                pw.w = __fmaf_rn(qq, s[j].w, pw.w);
+                pqk = __fmaf_rn(qq, kk, pqk);
             }
-        }
-        if (MODE == kReplayVerify && t + 1 == n_pre) {
-            // the replayed prefix is the new committed state; the new window is only verified
+            red_u[buf][rg][cg] = pu;
+            red_w[buf][rg][cg] = pw;
+            if (cg == 0) red_qk[buf][rg] = pqk;
+            __syncthreads();
+
+            float4 u = red_u[buf][0][cg], w = red_w[buf][0][cg];
+            float qk = red_qk[buf][0];
 #pragma unroll
-            for (int j = 0; j < RPT; ++j)
-                *reinterpret_cast<float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV) = s[j];
+            for (int r = 1; r < kRowGroups; ++r) {
+                const float4 ur = red_u[buf][r][cg], wr = red_w[buf][r][cg];
+                u.x = __fadd_rn(u.x, ur.x); u.y = __fadd_rn(u.y, ur.y);
+                u.z = __fadd_rn(u.z, ur.z); u.w = __fadd_rn(u.w, ur.w);
+                w.x = __fadd_rn(w.x, wr.x); w.y = __fadd_rn(w.y, wr.y);
+                w.z = __fadd_rn(w.z, wr.z); w.w = __fadd_rn(w.w, wr.w);
+                qk = __fadd_rn(qk, red_qk[buf][r]);
+            }
+            const float bt = sb[tt];
+            float4 d;
+            d.x = __fmul_rn(bt, __fsub_rn(sv[tt][cg * 4 + 0], u.x));
+            d.y = __fmul_rn(bt, __fsub_rn(sv[tt][cg * 4 + 1], u.y));
+            d.z = __fmul_rn(bt, __fsub_rn(sv[tt][cg * 4 + 2], u.z));
+            d.w = __fmul_rn(bt, __fsub_rn(sv[tt][cg * 4 + 3], u.w));
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) {
+                const float kk = sk[tt][rg + kRowGroups * j];
+                s[j].x = __fmaf_rn(kk, d.x, s[j].x);
+                s[j].y = __fmaf_rn(kk, d.y, s[j].y);
+                s[j].z = __fmaf_rn(kk, d.z, s[j].z);
+                s[j].w = __fmaf_rn(kk, d.w, s[j].w);
+            }
+            if (WRITE_O && t >= n_pre && rg == 0) {
+                float4 o;
+                o.x = __fmaf_rn(qk, d.x, w.x);
+                o.y = __fmaf_rn(qk, d.y, w.y);
+                o.z = __fmaf_rn(qk, d.z, w.z);
+                o.w = __fmaf_rn(qk, d.w, w.w);
+                const size_t oo = token_row(t) * DV + col0 + cg * 4;
+                if (p.o_bf16) {
+                    uint2 pk = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+                    *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.o) + oo) = pk;
+                } else {
+                    *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + oo) = o;
+                }
+            }
+            if (MODE == kReplayVerify && t + 1 == n_pre) {
+                // the replayed prefix is the new committed state; the new window is only verified
+#pragma unroll
+                for (int j = 0; j < RPT; ++j)
+                    *reinterpret_cast<float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV) = s[j];
+            }
         }
     }
 
-    if (MODE == kDecode || MODE == kReplay) {
+    if (COMMIT_END) {
 #pragma unroll
         for (int j = 0; j < RPT; ++j)
             *reinterpret_cast<float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV) = s[j];
@@ -299,7 +323,7 @@ struct PrevWindow {
 int run_kda(int mode, int B, int T, int H, int dk, int dv, float *S, const int32_t *state_idx,
             const hla_bf16 *q, const hla_bf16 *k, const hla_bf16 *v, const float *alpha,
             const float *beta, const int32_t *accepted, void *o, int o_dtype, cudaStream_t st,
-            const PrevWindow &prev = PrevWindow()) {
+            const PrevWindow &prev = PrevWindow(), const int32_t *cu_seqlens = nullptr) {
     HLA_REQUIRE(B >= 1 && H >= 1 && T >= 1, HLA_ERR_INVALID_ARG);
     HLA_REQUIRE(dk == dv && (dk == 64 || dk == 128), HLA_ERR_UNSUPPORTED);
     HLA_REQUIRE(T <= kMaxWindow, HLA_ERR_UNSUPPORTED);
@@ -307,6 +331,8 @@ int run_kda(int mode, int B, int T, int H, int dk, int dv, float *S, const int32
     HLA_REQUIRE(S && q && k && v && alpha && beta, HLA_ERR_INVALID_ARG);
     HLA_REQUIRE((mode != kReplay && mode != kReplayVerify) || accepted, HLA_ERR_INVALID_ARG);
     HLA_REQUIRE(mode == kReplay || o, HLA_ERR_INVALID_ARG);
+    HLA_REQUIRE(mode != kExtend || (cu_seqlens && aligned16(cu_seqlens)),
+                cu_seqlens ? HLA_ERR_MISALIGNED : HLA_ERR_INVALID_ARG);
     HLA_REQUIRE(o_dtype == HLA_F32 || o_dtype == HLA_BF16, HLA_ERR_INVALID_ARG);
     if (mode == kReplayVerify) {
         HLA_REQUIRE(prev.T >= 1, HLA_ERR_INVALID_ARG);
@@ -326,21 +352,24 @@ int run_kda(int mode, int B, int T, int H, int dk, int dv, float *S, const int32
     p.qp = prev.q; p.kp = prev.k; p.vp = prev.v; p.alphap = prev.alpha; p.betap = prev.beta;
     p.Tp = prev.T;
     p.accepted = accepted; p.o = o; p.o_bf16 = o_dtype == HLA_BF16; p.B = B; p.T = T; p.H = H;
+    p.cu_seqlens = cu_seqlens;
     int cw = choose_cw(B, H, dv);
     if (mode == kReplayVerify && cw > 64) cw = 64;  // two windows of token vectors in shared memory
-    static const char *names[4] = {"decode", "verify", "replay", "replay_verify"};
+    static const char *names[5] = {"decode", "verify", "replay", "replay_verify", "extend"};
     set_variant("kda_recur<dk%d,cw%d,%s>", dk, cw, names[mode]);
     int st_ = HLA_ERR_UNSUPPORTED;
     if (dk == 128) {
         st_ = mode == kDecode ? launch_dk<128, kDecode>(cw, p, st)
             : mode == kVerify ? launch_dk<128, kVerify>(cw, p, st)
             : mode == kReplay ? launch_dk<128, kReplay>(cw, p, st)
-                              : launch_dk<128, kReplayVerify>(cw, p, st);
+            : mode == kReplayVerify ? launch_dk<128, kReplayVerify>(cw, p, st)
+                                    : launch_dk<128, kExtend>(cw, p, st);
     } else {
         st_ = mode == kDecode ? launch_dk<64, kDecode>(cw, p, st)
             : mode == kVerify ? launch_dk<64, kVerify>(cw, p, st)
             : mode == kReplay ? launch_dk<64, kReplay>(cw, p, st)
-                              : launch_dk<64, kReplayVerify>(cw, p, st);
+            : mode == kReplayVerify ? launch_dk<64, kReplayVerify>(cw, p, st)
+                                    : launch_dk<64, kExtend>(cw, p, st);
     }
     return st_;
 }
@@ -395,6 +424,14 @@ extern "C" int kda_spec_replay_verify(int B, int T_prev, int T, int H, int dk, i
     prev.T = T_prev;
     return run_kda(kReplayVerify, B, T, H, dk, dv, S, state_idx, q, k, v, alpha, beta, accepted_prev,
                    o, o_dtype, (cudaStream_t)stream, prev);
+}
+
+extern "C" int kda_extend(int B, const int32_t *cu_seqlens, int H, int dk, int dv, float *S,
+                          const int32_t *state_idx, const hla_bf16 *q, const hla_bf16 *k,
+                          const hla_bf16 *v, const float *alpha, const float *beta, void *o,
+                          int o_dtype, hla_stream stream) {
+    return run_kda(kExtend, B, 1, H, dk, dv, S, state_idx, q, k, v, alpha, beta, nullptr, o,
+                   o_dtype, (cudaStream_t)stream, PrevWindow(), cu_seqlens);
 }
 
 extern "C" int spec_accept_prefix(int B, int T, const int32_t *draft_ids,

@@ -49,6 +49,7 @@ SIGNATURES = {
     "kda_spec_verify_replay": (c_int, [c_int] * 6 + [P] * 9 + [c_int, P]),
     "spec_accept_prefix": (c_int, [c_int, c_int] + [P] * 4 + [P]),
     "kda_spec_replay_verify": (c_int, [c_int] * 6 + [P] * 14 + [c_int, P]),
+    "kda_extend": (c_int, [c_int, P, c_int, c_int, c_int] + [P] * 8 + [c_int, P]),
     "skinny_proj_splitk_workspace_size": (c_size_t, [c_int] * 4),
     "skinny_proj_splitk": (c_int, [c_int] * 3 + [P] * 4 + [c_int, c_int, P, c_size_t, P]),
     "skinny_proj_residual_rmsnorm_workspace_size": (c_size_t, [c_int] * 4),
@@ -155,6 +156,13 @@ def kda_spec_replay_verify(B, T_prev, T, H, dk, dv, S, state_idx, q_prev, k_prev
         B, T_prev, T, H, dk, dv, _p(S), _p(state_idx), _p(q_prev), _p(k_prev), _p(v_prev),
         _p(alpha_prev), _p(beta_prev), _p(accepted_prev), _p(q), _p(k), _p(v), _p(alpha), _p(beta),
         _p(o), o_dtype, _stream(stream)))
+
+
+def kda_extend(B, cu_seqlens, H, dk, dv, S, state_idx, q, k, v, alpha, beta, o, o_dtype=HLA_F32,
+               stream=None):
+    return _check("kda_extend", load().kda_extend(
+        B, _p(cu_seqlens), H, dk, dv, _p(S), _p(state_idx), _p(q), _p(k), _p(v), _p(alpha),
+        _p(beta), _p(o), o_dtype, _stream(stream)))
 
 
 def spec_accept_prefix(B, T, draft_ids, target_ids, accepted_len, committed_len, stream=None):

@@ -153,6 +153,23 @@ int kda_spec_replay_verify(int B, int T_prev, int T, int H, int dk, int dv, floa
                            int o_dtype, hla_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * Mixed batch: every sequence brings its own number of new tokens (one for a decoding
+ * sequence, many for a prefill chunk).  [VLLM-K3] "What's Next": the decode path falls back
+ * seamlessly for prefills and mixed batches.
+ *  Sequence b owns the packed token rows cu_seqlens[b] .. cu_seqlens[b+1]-1; for every (b, h)
+ *  those tokens are applied in order to S[slot(b), h] (gated delta rule, as kda_decode_step),
+ *  o is written for every token, and the final state is stored.  A sequence with no tokens is
+ *  not touched.
+ *  cu_seqlens int32 [B + 1] (device, non-decreasing, cu_seqlens[0] = 0); q, k bf16 [N, H, dk];
+ *  v bf16 [N, H, dv]; alpha fp32 [N, H, dk]; beta fp32 [N, H]; o [N, H, dv] (o_dtype), where
+ *  N = cu_seqlens[B].  The tokens of one sequence are applied one after another with the state
+ *  held on chip (the recurrent form); every step is bit-identical to kda_decode_step.
+ * -------------------------------------------------------------------------*/
+int kda_extend(int B, const int32_t *cu_seqlens, int H, int dk, int dv, float *S,
+               const int32_t *state_idx, const hla_bf16 *q, const hla_bf16 *k, const hla_bf16 *v,
+               const float *alpha, const float *beta, void *o, int o_dtype, hla_stream stream);
+
+/* ---------------------------------------------------------------------------
  * Accepted-length bookkeeping.  [KIMI-WEBINAR] speculative decoding: greedy
  * acceptance of the drafted tokens the target agrees with.
  *  accepted_len[b]  = number of leading t with draft_ids[b,t] == target_ids[b,t]

@@ -132,3 +132,16 @@ def spec_replay_verify(S_c, prev, accepted_prev, new):
     S = spec_replay(S_c, prev["q"], prev["k"], prev["v"], prev["alpha"], prev["beta"], accepted_prev)
     o = spec_verify(S, new["q"], new["k"], new["v"], new["alpha"], new["beta"])
     return S, o
+
+
+def extend(S, cu_seqlens, q, k, v, alpha, beta):
+    """Mixed batch: sequence b applies its packed tokens cu_seqlens[b]..cu_seqlens[b+1]-1 in
+    order.  q, k, alpha [N, H, d_k]; v [N, H, d_v]; beta [N, H]; S [B, H, d_k, d_v].
+    Returns (new states, o [N, H, d_v])."""
+    S = f64(S).copy()
+    N = q.shape[0]
+    o = np.zeros((N,) + tuple(np.shape(v)[1:]))
+    for b in range(S.shape[0]):
+        for n in range(int(cu_seqlens[b]), int(cu_seqlens[b + 1])):
+            S[b], o[n] = kda_step(S[b], q[n], k[n], v[n], alpha[n], beta[n])
+    return S, o

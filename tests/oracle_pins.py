@@ -418,3 +418,45 @@ def fused_pin_failures(step, replay_verify):
             if not np.allclose(ot, o[b, t], rtol=1e-13, atol=1e-13):
                 fails.append("fused outputs equal sequential steps from the new committed state")
     return sorted(set(fails))
+
+
+# --------------------------------------------------------------------------------------
+# mixed batch (packed ragged sequences)
+# --------------------------------------------------------------------------------------
+
+def extend_pin_failures(step, extend):
+    fails = []
+    exs = _load("kda_worked_examples.json")["examples"]
+    e1, e3 = exs[0], exs[2]
+    # one sequence of two tokens (example 1 then example 3) and one empty sequence
+    S = np.array([[e1["S"]], [[[9.0, 9.0], [9.0, 9.0]]]], float)          # [B=2, H=1, 2, 2]
+    q = np.array([[e1["q"]], [e3["q"]]], float)                            # [N=2, H=1, 2]
+    k = np.array([[e1["k"]], [e3["k"]]], float)
+    v = np.array([[e1["v"]], [e3["v"]]], float)
+    al = np.array([[e1["alpha"]], [e3["alpha"]]], float)
+    be = np.array([[e1["beta"]], [e3["beta"]]], float)
+    S_new, o = extend(S, np.array([0, 2, 2]), q, k, v, al, be)
+    if not (np.array_equal(S_new[0, 0], np.array(e3["S_t"], float))
+            and np.array_equal(o[0, 0], np.array(e1["o"], float))
+            and np.array_equal(o[1, 0], np.array(e3["o"], float))):
+        fails.append("extend golden chain")
+    if not np.array_equal(S_new[1], S[1]):
+        fails.append("extend leaves an empty sequence untouched")
+
+    rng = _rng(31)
+    H, dk, dv = 2, 3, 4
+    cu = np.array([0, 3, 3, 4, 9])
+    B, N = len(cu) - 1, cu[-1]
+    S = rng.standard_normal((B, H, dk, dv))
+    q, k = rng.standard_normal((N, H, dk)), rng.standard_normal((N, H, dk))
+    v, al, be = rng.standard_normal((N, H, dv)), rng.uniform(0.1, 0.9, (N, H, dk)), rng.uniform(0, 1, (N, H))
+    S_new, o = extend(S, cu, q, k, v, al, be)
+    for b in range(B):
+        Sb = S[b].copy()
+        for n in range(cu[b], cu[b + 1]):
+            Sb, on = step(Sb, q[n], k[n], v[n], al[n], be[n])
+            if not np.allclose(on, o[n], rtol=1e-13, atol=1e-13):
+                fails.append("extend outputs equal sequential steps")
+        if not np.allclose(Sb, S_new[b], rtol=1e-13, atol=1e-13):
+            fails.append("extend states equal sequential steps")
+    return sorted(set(fails))

@@ -233,3 +233,57 @@ def test_fused_replay_verify(dev, B, Tp, T, d, acc_kind):
     for b in range(B):
         if int(acc[b]) == 0:
             assert torch.equal(S1[b].cpu(), S0[b])
+
+
+def test_extend_single_tokens_equal_decode_bitwise(dev):
+    B, H, d = 8, 32, 128
+    S0 = warm_states(1, B, H, d)
+    inp = _to(inputs.kda_inputs((B,), H, d, d, inputs.generator(81)), dev)
+    S1, S2 = S0.to(dev), S0.to(dev)
+    o1 = _decode(dev, S1, inp)
+    o2 = torch.empty(B, H, d, device=dev)
+    cu = torch.arange(B + 1, dtype=torch.int32, device=dev)
+    hla.kda_extend(B, cu, H, d, d, S2, None, inp["q"], inp["k"], inp["v"], inp["alpha"], inp["beta"], o2)
+    torch.cuda.synchronize()
+    assert "extend" in hla.hla_last_variant()
+    assert torch.equal(S1, S2) and torch.equal(o1, o2)
+
+
+@pytest.mark.parametrize("lens,d", [([0, 1, 5, 17, 3, 40, 8, 1], 128), ([2, 0, 9], 64)])
+def test_extend_ragged_mixed_batch(dev, lens, d):
+    """Ragged sequences (empty, single-token decode, multi-block prefill chunks) in one call:
+    against the oracle, and bitwise against one decode call per token."""
+    B = len(lens)
+    H = 32 if d == 128 else 4
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(cu[-1])
+    S0 = warm_states(8, B, H, d)
+    tok = inputs.kda_inputs((N,), H, d, d, inputs.generator(82 + N))
+    perm = torch.randperm(B + 3, generator=inputs.generator(83))[:B].to(torch.int32)
+    pool = torch.zeros(B + 3, H, d, d)
+    pool[perm.long()] = S0
+    S = pool.to(dev)
+    td = _to(tok, dev)
+    o = torch.empty(N, H, d, device=dev)
+    hla.kda_extend(B, torch.from_numpy(cu).to(dev), H, d, d, S, perm.to(dev), td["q"], td["k"], td["v"],
+                   td["alpha"], td["beta"], o)
+    torch.cuda.synchronize()
+    S_ref, o_ref = oracle.kda.extend(f64(S0), cu, *(f64(tok[key]) for key in ("q", "k", "v", "alpha", "beta")))
+    got = S.cpu()[perm.long()]
+    assert max_rel(got.double().numpy(), S_ref) < KDA_MAX_REL
+    assert max_rel(f64(o), o_ref) < KDA_MAX_REL
+    for b in range(B):
+        if lens[b] == 0:
+            assert torch.equal(got[b], S0[b])
+    # bitwise against single decode steps, one sequence at a time
+    S2 = pool.to(dev)
+    o2 = torch.empty(N, H, d, device=dev)
+    for b in range(B):
+        for n in range(cu[b], cu[b + 1]):
+            step = {key: val[n:n + 1].contiguous() for key, val in td.items()}
+            ob = torch.empty(1, H, d, device=dev)
+            hla.kda_decode_step(1, H, d, d, S2, perm[b:b + 1].to(dev), step["q"], step["k"], step["v"],
+                                step["alpha"], step["beta"], ob)
+            o2[n] = ob[0]
+    torch.cuda.synchronize()
+    assert torch.equal(S2, S) and torch.equal(o2, o)

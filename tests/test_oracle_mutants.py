@@ -10,7 +10,8 @@ import pytest
 from oracle import kda, moe, layer, numerics
 from oracle.numerics import f64, sigmoid, silu
 from tests.oracle_pins import (kda_pin_failures, spec_pin_failures, moe_pin_failures,
-                               layer_pin_failures, fused_pin_failures)
+                               layer_pin_failures, fused_pin_failures,
+                               extend_pin_failures)
 
 
 def _caught(fn, *args):
@@ -245,3 +246,23 @@ def _fused_replays_all(S_c, prev, acc, new):
 @pytest.mark.parametrize("mutant", [_fused_verifies_stale_state, _fused_replays_all])
 def test_fused_mutants_are_caught(mutant):
     assert _caught(fused_pin_failures, kda.kda_step, mutant)
+
+
+def _extend_off_by_one_offsets(S, cu, q, k, v, alpha, beta):
+    cu = np.asarray(cu).copy()
+    cu[1:-1] += 1  # sequences take one token of their successor
+    return kda.extend(S, cu, q, k, v, alpha, beta)
+
+
+def _extend_reversed(S, cu, q, k, v, alpha, beta):
+    S = np.asarray(S, float).copy()
+    o = np.zeros((q.shape[0],) + tuple(np.shape(v)[1:]))
+    for b in range(S.shape[0]):
+        for n in reversed(range(int(cu[b]), int(cu[b + 1]))):
+            S[b], o[n] = kda.kda_step(S[b], q[n], k[n], v[n], alpha[n], beta[n])
+    return S, o
+
+
+@pytest.mark.parametrize("mutant", [_extend_off_by_one_offsets, _extend_reversed])
+def test_extend_mutants_are_caught(mutant):
+    assert _caught(extend_pin_failures, kda.kda_step, mutant)

@@ -5,7 +5,8 @@ import numpy as np
 import oracle
 from oracle import kda, moe, layer, numerics
 from tests.oracle_pins import (kda_pin_failures, spec_pin_failures, moe_pin_failures,
-                               layer_pin_failures, fused_pin_failures)
+                               layer_pin_failures, fused_pin_failures,
+                               extend_pin_failures)
 
 
 def test_kda_step_pins():
@@ -18,6 +19,10 @@ def test_spec_window_pins():
 
 def test_fused_replay_verify_pins():
     assert fused_pin_failures(kda.kda_step, kda.spec_replay_verify) == []
+
+
+def test_extend_pins():
+    assert extend_pin_failures(kda.kda_step, kda.extend) == []
 
 
 def test_moe_pins():
