@@ -64,31 +64,49 @@ struct MoeArgs {
 
 int moe_tokens_per_tile(int M) { return M <= 8 ? 8 : 16; }
 
-// K slices of the down projection: only at the smallest batches, where the (units x 32-row
-// blocks) items alone leave each SM with a single wave of 128 KB items.
-int moe_down_split(int M, int Hd, int E, int k, int nsh) {
+// K splits of the expert products.  Two rules, the larger wins:
+//  * enough work items: about 24 warp items per SM (units x row blocks x split);
+//  * short items at small batch: with the 8-token tile (batch <= 8) a gate/up item is cut
+//    to about 128 KB of weights and a down item to about 64 KB, so that the last items
+//    claimed end soon after the others (at batch 8: 726 us with splits 4 / 2 against 775 us
+//    unsplit; at batch 32 and 64 splitting measured no better or slower, the partials then
+//    being large).
+int moe_items_split(int M, int k, int E, int nsh, long row_blocks, long cap) {
     long units = (long)M * k < E ? (long)M * k : E;
     units += nsh;
-    const long items = units * ((Hd + 31) / 32);
+    const long items = units * row_blocks;
     long s = (24L * sm_count() + items - 1) / items;
     if (s < 1) s = 1;
-    if (s > 4) s = 4;
-    return (int)s;
+    return (int)(s > cap ? cap : s);
 }
 
-int moe_gateup_split(int M, int I, int E, int k, int nsh) {
+int moe_bytes_split(int M, long item_bytes, long target, long cap) {
+    if (M > 8) return 1;
+    long s = (item_bytes + target - 1) / target;
+    if (s < 1) s = 1;
+    return (int)(s > cap ? cap : s);
+}
+
+int moe_down_split(int M, int Hd, int I, int E, int k, int nsh) {
+    const char *env = getenv("HLA_MOE_DOWN_SPLIT");
+    if (env) {
+        const int v = atoi(env);
+        if (v >= 1 && v <= 4) return v;
+    }
+    const int a = moe_items_split(M, k, E, nsh, (Hd + 31) / 32, 4);
+    const int b = moe_bytes_split(M, 32L * I * 2, 64L * 1024, 4);  // 32 rows of W_down
+    return a > b ? a : b;
+}
+
+int moe_gateup_split(int M, int Hd, int I, int E, int k, int nsh) {
     const char *env = getenv("HLA_MOE_SPLIT");
     if (env) {
         const int v = atoi(env);
         if (v >= 1 && v <= 16) return v;
     }
-    long units = (long)M * k < E ? (long)M * k : E;
-    units += nsh;
-    const long items = units * ((I + 15) / 16);
-    long s = (24L * sm_count() + items - 1) / items;
-    if (s < 1) s = 1;
-    if (s > 8) s = 8;
-    return (int)s;
+    const int a = moe_items_split(M, k, E, nsh, (I + 15) / 16, 8);
+    const int b = moe_bytes_split(M, 2L * 16 * Hd * 2, 128L * 1024, 8);  // 16 rows of W_gate and W_up
+    return a > b ? a : b;
 }
 
 MoeLayout moe_layout(int M, int Hd, int I, int E, int k, int nsh) {
@@ -96,8 +114,8 @@ MoeLayout moe_layout(int M, int Hd, int I, int E, int k, int nsh) {
     L.M = M; L.Hd = Hd; L.I = I; L.E = E; L.k = k; L.nsh = nsh;
     L.P = M * (k + nsh);
     L.U_max = E + nsh;
-    L.KS = moe_gateup_split(M, I, E, k, nsh);
-    L.KSD = moe_down_split(M, Hd, E, k, nsh);
+    L.KS = moe_gateup_split(M, Hd, I, E, k, nsh);
+    L.KSD = moe_down_split(M, Hd, I, E, k, nsh);
     L.TT = moe_tokens_per_tile(M);
     // Optional (HLA_SHARED_TC=1): past 16 tokens run each shared expert as a dense SwiGLU
     // over all M tokens on the tensor-core path instead of as a grouped work unit.  Off by
@@ -131,9 +149,10 @@ MoeLayout moe_layout(int M, int Hd, int I, int E, int k, int nsh) {
     return L;
 }
 
-// Exclusive prefix sum over one value per thread of a kDispatchThreads-thread block.
+// Exclusive prefix sum over one value per thread of the block (a whole number of warps,
+// at most 1024 threads).
 __device__ int block_exclusive_scan(int v, int *warp_tot, int &total) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
     int incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -144,7 +163,7 @@ __device__ int block_exclusive_scan(int v, int *warp_tot, int &total) {
     if (lane == 31) warp_tot[w] = incl;
     __syncthreads();
     if (w == 0) {
-        const int t = warp_tot[lane];
+        const int t = lane < nw ? warp_tot[lane] : 0;
         int s = t;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -159,6 +178,7 @@ __device__ int block_exclusive_scan(int v, int *warp_tot, int &total) {
     return warp_tot[w] + incl - v;
 }
 
+// One CTA of round_up(E + n_shared, 32) threads (thread e owns expert e's count and unit).
 __global__ void __launch_bounds__(kDispatchThreads) moe_dispatch_kernel(const MoeArgs a) {
     __shared__ int cnt[1024], base[1024], run[1024], uid[1024];
     __shared__ int warp_tot[33];
@@ -169,7 +189,7 @@ __global__ void __launch_bounds__(kDispatchThreads) moe_dispatch_kernel(const Mo
     cnt[tid] = 0;
     run[tid] = 0;
     __syncthreads();
-    for (int p = tid; p < npairs; p += kDispatchThreads) {
+    for (int p = tid; p < npairs; p += blockDim.x) {
         const int e = a.topk_idx[p];
         if (e >= 0 && e < a.E) atomicAdd(&cnt[e], 1);
     }
@@ -200,7 +220,7 @@ __global__ void __launch_bounds__(kDispatchThreads) moe_dispatch_kernel(const Mo
             __syncwarp();
         }
     }
-    for (int i = tid; i < routed0; i += kDispatchThreads) {
+    for (int i = tid; i < routed0; i += blockDim.x) {
         const int s = i / a.M, m = i % a.M;
         a.pos_token[i] = m;
         a.pos_slot[i] = m * (a.k + a.nsh) + a.k + s;
@@ -330,6 +350,7 @@ __global__ void moe_swiglu_reduce_kernel(const MoeArgs a) {
     for (size_t i = first + blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
         float g = a.part_g[i], u = a.part_u[i];
+#pragma unroll 4
         for (int s = 1; s < a.KS; ++s) {
             g = __fadd_rn(g, a.part_g[s * plane + i]);
             u = __fadd_rn(u, a.part_u[s * plane + i]);
@@ -392,32 +413,53 @@ __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(const MoeArgs a) 
     }
 }
 
+// y[m] = sum_j w[m,j] * (sum over down slices of y[m,j]) (+ residual): slots in increasing
+// order, slices in increasing order.  Slots are taken four at a time with their routing
+// entries and all their slice rows loaded before any of them is used, so each group of four
+// slots costs one round of memory latency.
 __global__ void moe_combine_kernel(const MoeArgs a) {
     const int m = blockIdx.y;
     const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
     if (c4 * 4 >= a.Hd) return;
     const int S = a.k + a.nsh;
+    const size_t plane = (size_t)a.P * a.Hd;
+    const float *base = a.ypart + (size_t)m * S * a.Hd + (size_t)c4 * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < S; ++j) {
-        float w = 1.0f;
-        if (j < a.k) {
-            const int e = a.topk_idx[(size_t)m * a.k + j];
-            if (e < 0 || e >= a.E) continue;
-            w = a.topk_w[(size_t)m * a.k + j];
+    for (int j0 = 0; j0 < S; j0 += 4) {
+        float4 v[4][4];
+        int e[4];
+        float w[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = j0 + jj;
+            const bool routed = j < a.k;
+            e[jj] = routed ? a.topk_idx[(size_t)m * a.k + j] : 0;
+            w[jj] = routed ? a.topk_w[(size_t)m * a.k + j] : 1.0f;
+            const int nks = (j >= a.k && a.nsh_units == 0) ? 1 : a.KSD;  // tensor-core shared slot: one plane
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                v[jj][ks] = (j < S && ks < nks)
+                                ? *reinterpret_cast<const float4 *>(base + ks * plane + (size_t)j * a.Hd)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const bool tc_slot = j >= a.k && a.nsh_units == 0;
-        const int nks = tc_slot ? 1 : a.KSD;
-        float4 v = reinterpret_cast<const float4 *>(a.ypart + ((size_t)m * S + j) * a.Hd)[c4];
-        for (int ks = 1; ks < nks; ++ks) {
-            const float4 t = reinterpret_cast<const float4 *>(
-                a.ypart + ((size_t)ks * a.P + (size_t)m * S + j) * a.Hd)[c4];
-            v.x = __fadd_rn(v.x, t.x); v.y = __fadd_rn(v.y, t.y);
-            v.z = __fadd_rn(v.z, t.z); v.w = __fadd_rn(v.w, t.w);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = j0 + jj;
+            if (j >= S) break;
+            if (j < a.k && (e[jj] < 0 || e[jj] >= a.E)) continue;
+            const int nks = (j >= a.k && a.nsh_units == 0) ? 1 : a.KSD;
+            float4 t = v[jj][0];
+#pragma unroll
+            for (int ks = 1; ks < 4; ++ks) {
+                if (ks >= nks) break;
+                t.x = __fadd_rn(t.x, v[jj][ks].x); t.y = __fadd_rn(t.y, v[jj][ks].y);
+                t.z = __fadd_rn(t.z, v[jj][ks].z); t.w = __fadd_rn(t.w, v[jj][ks].w);
+            }
+            acc.x = __fmaf_rn(w[jj], t.x, acc.x);
+            acc.y = __fmaf_rn(w[jj], t.y, acc.y);
+            acc.z = __fmaf_rn(w[jj], t.z, acc.z);
+            acc.w = __fmaf_rn(w[jj], t.w, acc.w);
         }
-        acc.x = __fmaf_rn(w, v.x, acc.x);
-        acc.y = __fmaf_rn(w, v.y, acc.y);
-        acc.z = __fmaf_rn(w, v.z, acc.z);
-        acc.w = __fmaf_rn(w, v.w, acc.w);
     }
     const size_t o = (size_t)m * a.Hd + (size_t)c4 * 4;
     if (a.residual) {
@@ -553,7 +595,8 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
             if ((r = launch_status()) != HLA_OK) return r;
         }
     }
-    moe_dispatch_kernel<<<1, kDispatchThreads, 0, st>>>(a);
+    const int dthreads = (int)round_up((size_t)(E + nsh), 32);
+    moe_dispatch_kernel<<<1, dthreads, 0, st>>>(a);
     r = launch_status();
     if (r != HLA_OK) return r;
     trace_before(kTraceMoeGateup, st);
