@@ -63,6 +63,17 @@ LayerLayout layer_layout(const hla_layer *L, int M) {
 thread_local cudaEvent_t g_fork = nullptr, g_join = nullptr;
 
 }  // namespace
+
+bool moe_shared_on_side(int M, int nsh, bool have_side);
+int moe_shared_side(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x,
+                    const hla_bf16 *Ws_gate, const hla_bf16 *Ws_up, const hla_bf16 *Ws_down,
+                    void *ws, cudaStream_t st, cudaStream_t side);
+int moe_forward_checked(int M, int Hd, int I, int E, int k, int n_shared, const hla_bf16 *x,
+                        const int32_t *topk_idx, const float *topk_w, const hla_bf16 *W_gate,
+                        const hla_bf16 *W_up, const hla_bf16 *W_down, const hla_bf16 *Ws_gate,
+                        const hla_bf16 *Ws_up, const hla_bf16 *Ws_down, const hla_bf16 *residual,
+                        hla_bf16 *y, void *ws, size_t ws_bytes, cudaStream_t st, cudaStream_t pf,
+                        bool shared_external);
 }  // namespace hla
 
 using namespace hla;
@@ -116,14 +127,22 @@ extern "C" int hla_decode_layer(const hla_layer *L, int M, const hla_bf16 *x, fl
                                           bf(lo.r), bf(lo.x2), 0, w + lo.oproj_ws, lo.oproj_bytes,
                                           stream)) != HLA_OK)
         return r;
+    // The shared experts do not depend on the routing: when they run on the side stream they
+    // start here, overlapping the router and dispatch ("Hyper-optimizing Kimi K3 in vLLM",
+    // Part 1 sec. 3).
+    const bool shared_side = moe_shared_on_side(M, L->n_shared, pf != nullptr);
+    if (shared_side &&
+        (r = moe_shared_side(M, Hd, L->inter, L->n_experts, L->top_k, L->n_shared, bf(lo.x2),
+                             L->Ws_gate, L->Ws_up, L->Ws_down, w + lo.moe_ws, st, pf)) != HLA_OK)
+        return r;
     if ((r = moe_route_topk(M, Hd, L->n_experts, L->top_k, bf(lo.x2), L->W_router,
                             reinterpret_cast<int32_t *>(w + lo.idx), f32(lo.w), nullptr,
                             w + lo.router_ws, lo.router_bytes, stream)) != HLA_OK)
         return r;
-    if ((r = moe_expert_forward(M, Hd, L->inter, L->n_experts, L->top_k, L->n_shared, bf(lo.x2),
-                                reinterpret_cast<int32_t *>(w + lo.idx), f32(lo.w), L->W_gate,
-                                L->W_up, L->W_down, L->Ws_gate, L->Ws_up, L->Ws_down, bf(lo.r), y,
-                                w + lo.moe_ws, lo.moe_bytes, stream, prefetch_stream)) != HLA_OK)
+    if ((r = moe_forward_checked(M, Hd, L->inter, L->n_experts, L->top_k, L->n_shared, bf(lo.x2),
+                                 reinterpret_cast<int32_t *>(w + lo.idx), f32(lo.w), L->W_gate,
+                                 L->W_up, L->W_down, L->Ws_gate, L->Ws_up, L->Ws_down, bf(lo.r), y,
+                                 w + lo.moe_ws, lo.moe_bytes, st, pf, shared_side)) != HLA_OK)
         return r;
     if (layer_pf && cudaStreamWaitEvent(st, g_join, 0) != cudaSuccess) return HLA_ERR_CUDA;
     set_variant("decode_layer%s", pf ? "<prefetch>" : "");

@@ -32,6 +32,9 @@ namespace hla {
 
 int run_l2_prefetch(const void *ptr, size_t bytes, cudaStream_t st);
 int dense_tc_split(int M, int N, int K);
+int dense_auto_split(int M, int N, int K);
+int run_dense(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W, int split, float *part,
+              void *y, int y_bf16, const hla_bf16 *residual, cudaStream_t st);
 int run_dense_tc(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W, int split, float *part,
                  void *y, int y_bf16, const hla_bf16 *residual, cudaStream_t st);
 
@@ -44,6 +47,7 @@ struct MoeLayout {
     int M, Hd, I, E, k, nsh, P, U_max, KS, KSD, TT;
     bool shared_tc;      // shared experts on the tensor-core path instead of grouped work units
     int s_gu, s_dn;      // K slices of the shared experts' tensor-core products
+    int d_gu, d_dn;      // K slices of the shared experts' products when they run on a side stream
     size_t off_meta, off_unit_expert, off_unit_off, off_item_gu, off_item_dn, off_pos_token,
         off_pos_slot, off_h, off_part_g, off_part_u, off_ypart, off_sh_g, off_sh_u, off_sh_d, total;
 };
@@ -125,6 +129,12 @@ MoeLayout moe_layout(int M, int Hd, int I, int E, int k, int nsh) {
     L.shared_tc = nsh > 0 && M > 16 && env && env[0] == '1';
     L.s_gu = L.shared_tc ? dense_tc_split(M, I, Hd) : 0;
     L.s_dn = L.shared_tc ? dense_tc_split(M, Hd, I) : 0;
+    // The side-stream placement (moe_shared_side) can be chosen per call, so its partial
+    // buffers are always part of the workspace when there are shared experts.
+    L.d_gu = nsh > 0 ? dense_auto_split(M, I, Hd) : 0;
+    L.d_dn = nsh > 0 ? dense_auto_split(M, Hd, I) : 0;
+    const size_t sgu = (size_t)(L.s_gu > L.d_gu ? L.s_gu : L.d_gu);
+    const size_t sdn = (size_t)(L.s_dn > L.d_dn ? L.s_dn : L.d_dn);
     size_t o = 0;
     auto take = [&](size_t bytes) {
         const size_t at = o;
@@ -142,9 +152,9 @@ MoeLayout moe_layout(int M, int Hd, int I, int E, int k, int nsh) {
     L.off_part_g = take(L.KS > 1 ? (size_t)L.KS * L.P * I * sizeof(float) : 0);
     L.off_part_u = take(L.KS > 1 ? (size_t)L.KS * L.P * I * sizeof(float) : 0);
     L.off_ypart = take((size_t)L.KSD * L.P * Hd * sizeof(float));
-    L.off_sh_g = take(L.shared_tc ? (size_t)L.s_gu * M * I * sizeof(float) : 0);
-    L.off_sh_u = take(L.shared_tc ? (size_t)L.s_gu * M * I * sizeof(float) : 0);
-    L.off_sh_d = take(L.shared_tc ? (size_t)L.s_dn * M * Hd * sizeof(float) : 0);
+    L.off_sh_g = take(sgu * M * I * sizeof(float));
+    L.off_sh_u = take(sgu * M * I * sizeof(float));
+    L.off_sh_d = take(sdn * M * Hd * sizeof(float));
     L.total = o;
     return L;
 }
@@ -502,6 +512,16 @@ __global__ void shared_down_reduce_kernel(const float *__restrict__ pd, int spli
     }
 }
 
+// SMs withheld from the routed experts' persistent grids while the shared experts run on the
+// side stream, so that the side kernels find free SMs (HLA_SHARED_SM_BUDGET overrides the
+// default of 16: at batch 8 the layer took 1029 us with no SMs withheld, 926 us with 16,
+// 924 us with 38 and 1110 us with 76; at batch 1 and 2, 16 was best by a small margin).
+int shared_sm_budget() {
+    const char *env = getenv("HLA_SHARED_SM_BUDGET");
+    const int b = env ? atoi(env) : 16;
+    return b < 0 ? 0 : (b > sm_count() / 2 ? sm_count() / 2 : b);
+}
+
 template <typename K>
 int persistent_grid(K kernel) {
     int per_sm = 0;
@@ -521,23 +541,94 @@ struct SideStreamEvents {
 };
 thread_local SideStreamEvents g_moe_events;
 
+
+// The shared experts as dense SwiGLUs over all M tokens: gate and up products (split K,
+// fp32 slices), h = SiLU(sum g) * (sum u) into the shared experts' h rows, the down product,
+// and its slice sum into the shared slots of the expert-output rows (one plane), where the
+// combine reads them.  tc: the tensor-core tiles (the optional path at more than 16 tokens);
+// otherwise the projection entry point's own choice of path and split.
+int run_shared_dense(const MoeLayout &L, bool tc, const hla_bf16 *x, const hla_bf16 *Ws_gate,
+                     const hla_bf16 *Ws_up, const hla_bf16 *Ws_down, char *w, cudaStream_t st) {
+    const int M = L.M, Hd = L.Hd, I = L.I;
+    float *pg = reinterpret_cast<float *>(w + L.off_sh_g);
+    float *pu = reinterpret_cast<float *>(w + L.off_sh_u);
+    float *pd = reinterpret_cast<float *>(w + L.off_sh_d);
+    uint16_t *h = reinterpret_cast<uint16_t *>(w + L.off_h);
+    float *ypart = reinterpret_cast<float *>(w + L.off_ypart);
+    const int sgu = tc ? L.s_gu : L.d_gu, sdn = tc ? L.s_dn : L.d_dn;
+    const int grid = 2 * sm_count();
+    auto proj = [&](int N, int K, const hla_bf16 *in, const hla_bf16 *W, int split, float *part) {
+        return tc ? run_dense_tc(M, N, K, in, W, split, part, nullptr, 0, nullptr, st)
+                  : run_dense(M, N, K, in, W, split, part, nullptr, 0, nullptr, st);
+    };
+    int r;
+    for (int s = 0; s < L.nsh; ++s) {
+        const size_t eo = (size_t)s * I * Hd;
+        hla_bf16 *hs = h + (size_t)s * M * I;
+        if ((r = proj(I, Hd, x, Ws_gate + eo, sgu, pg)) != HLA_OK) return r;
+        if ((r = proj(I, Hd, x, Ws_up + eo, sgu, pu)) != HLA_OK) return r;
+        shared_swiglu_kernel<<<grid, 256, 0, st>>>(pg, pu, sgu, M, I, hs);
+        if ((r = launch_status()) != HLA_OK) return r;
+        if ((r = proj(Hd, I, hs, Ws_down + eo, sdn, pd)) != HLA_OK) return r;
+        shared_down_reduce_kernel<<<grid, 256, 0, st>>>(pd, sdn, M, Hd, L.k + L.nsh, L.k + s, ypart);
+        if ((r = launch_status()) != HLA_OK) return r;
+    }
+    return HLA_OK;
+}
+
+thread_local SideStreamEvents g_shared_events;
+
 }  // namespace
 
 size_t moe_workspace_bytes(int M, int Hd, int I, int E, int k, int nsh) {
     return moe_layout(M, Hd, I, E, k, nsh).total;
 }
 
+// Whether the shared experts run on the side stream, overlapping the router, dispatch and
+// the routed experts ("Hyper-optimizing Kimi K3 in vLLM", Part 1 sec. 3: the shared expert
+// does not depend on the routing).  Needs a side stream; the tensor-core shared path
+// (HLA_SHARED_TC=1) takes precedence.  Off unless HLA_SHARED_STREAM=1: in the decode layer
+// (CUDA graph, 16 SMs withheld from the routed kernels) it measured 212 vs 210 us at batch 1,
+// 319 vs 321 us at batch 2, 926 vs 909 us at batch 8, and at batch 64 (no SMs withheld)
+// 3980 vs 3105 us, where the grouped unit also profits from the L2 warming of its rows.
+bool moe_shared_on_side(int M, int nsh, bool have_side) {
+    if (nsh <= 0 || !have_side) return false;
+    const char *tc = getenv("HLA_SHARED_TC");
+    if (M > 16 && tc && tc[0] == '1') return false;
+    const char *env = getenv("HLA_SHARED_STREAM");
+    return env && env[0] == '1';
+}
+
+// Fork the shared experts onto `side` (after everything already queued on `st`); their
+// outputs land in the workspace, and run_moe(..., shared_external = true) joins before its
+// combine.  The side stream only touches the shared experts' partial buffers, h rows and
+// output slots, which no routed kernel reads or writes.
+int moe_shared_side(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x,
+                    const hla_bf16 *Ws_gate, const hla_bf16 *Ws_up, const hla_bf16 *Ws_down,
+                    void *ws, cudaStream_t st, cudaStream_t side) {
+    const MoeLayout L = moe_layout(M, Hd, I, E, k, nsh);
+    if (!g_shared_events.ok()) return HLA_ERR_CUDA;
+    if (cudaEventRecord(g_shared_events.fork, st) != cudaSuccess) return HLA_ERR_CUDA;
+    if (cudaStreamWaitEvent(side, g_shared_events.fork, 0) != cudaSuccess) return HLA_ERR_CUDA;
+    const int r = run_shared_dense(L, false, x, Ws_gate, Ws_up, Ws_down, reinterpret_cast<char *>(ws),
+                                   side);
+    if (r != HLA_OK) return r;
+    if (cudaEventRecord(g_shared_events.join, side) != cudaSuccess) return HLA_ERR_CUDA;
+    return HLA_OK;
+}
+
 int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, const int32_t *topk_idx,
             const float *topk_w, const hla_bf16 *W_gate, const hla_bf16 *W_up,
             const hla_bf16 *W_down, const hla_bf16 *Ws_gate, const hla_bf16 *Ws_up,
             const hla_bf16 *Ws_down, const hla_bf16 *residual, hla_bf16 *y, void *ws,
-            cudaStream_t st, cudaStream_t pf) {
+            cudaStream_t st, cudaStream_t pf, bool shared_external) {
     const MoeLayout L = moe_layout(M, Hd, I, E, k, nsh);
+    const bool shared_side = shared_external || moe_shared_on_side(M, nsh, pf != nullptr);
     char *w = reinterpret_cast<char *>(ws);
     MoeArgs a;
     a.M = M; a.Hd = Hd; a.I = I; a.E = E; a.k = k; a.nsh = nsh; a.P = L.P; a.KS = L.KS; a.TT = L.TT;
     a.KSD = L.KSD;
-    a.nsh_units = L.shared_tc ? 0 : nsh;
+    a.nsh_units = (L.shared_tc || shared_side) ? 0 : nsh;
     a.x = x; a.topk_idx = topk_idx; a.topk_w = topk_w;
     a.W_gate = W_gate; a.W_up = W_up; a.W_down = W_down;
     a.Ws_gate = Ws_gate; a.Ws_up = Ws_up; a.Ws_down = Ws_down;
@@ -560,8 +651,8 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     // (measured +11% per layer at batch 1, +19% at batch 8).
     const int pm = prefetch_mask();
     const int mask = pm >= 0 ? pm & (kPrefetchSharedGateUp | kPrefetchSharedDown)
-                             : ((!L.shared_tc && M > L.TT) ? kPrefetchSharedGateUp : 0);
-    const bool side = pf != nullptr && nsh > 0 && mask != 0;
+                             : ((a.nsh_units > 0 && M > L.TT) ? kPrefetchSharedGateUp : 0);
+    const bool side = pf != nullptr && nsh > 0 && mask != 0 && !shared_side;
     if (side) {
         if (!g_moe_events.ok()) return HLA_ERR_CUDA;
         if (cudaEventRecord(g_moe_events.fork, st) != cudaSuccess) return HLA_ERR_CUDA;
@@ -579,35 +670,26 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
 
     int r;
     if (L.shared_tc) {
-        float *pg = reinterpret_cast<float *>(w + L.off_sh_g);
-        float *pu = reinterpret_cast<float *>(w + L.off_sh_u);
-        float *pd = reinterpret_cast<float *>(w + L.off_sh_d);
-        const int grid = 2 * sm_count();
-        for (int s = 0; s < nsh; ++s) {
-            const size_t eo = (size_t)s * I * Hd;
-            hla_bf16 *hs = a.h + (size_t)s * M * I;
-            if ((r = run_dense_tc(M, I, Hd, x, Ws_gate + eo, L.s_gu, pg, nullptr, 0, nullptr, st)) != HLA_OK) return r;
-            if ((r = run_dense_tc(M, I, Hd, x, Ws_up + eo, L.s_gu, pu, nullptr, 0, nullptr, st)) != HLA_OK) return r;
-            shared_swiglu_kernel<<<grid, 256, 0, st>>>(pg, pu, L.s_gu, M, I, hs);
-            if ((r = launch_status()) != HLA_OK) return r;
-            if ((r = run_dense_tc(M, Hd, I, hs, Ws_down + eo, L.s_dn, pd, nullptr, 0, nullptr, st)) != HLA_OK) return r;
-            shared_down_reduce_kernel<<<grid, 256, 0, st>>>(pd, L.s_dn, M, Hd, k + nsh, k + s, a.ypart);
-            if ((r = launch_status()) != HLA_OK) return r;
-        }
+        if ((r = run_shared_dense(L, true, x, Ws_gate, Ws_up, Ws_down, w, st)) != HLA_OK) return r;
+    } else if (shared_side && !shared_external) {
+        if ((r = moe_shared_side(M, Hd, I, E, k, nsh, x, Ws_gate, Ws_up, Ws_down, ws, st, pf)) != HLA_OK)
+            return r;
     }
     const int dthreads = (int)round_up((size_t)(E + nsh), 32);
     moe_dispatch_kernel<<<1, dthreads, 0, st>>>(a);
     r = launch_status();
     if (r != HLA_OK) return r;
+    const int keep = shared_side ? sm_count() - shared_sm_budget() : sm_count();
+    auto budgeted = [&](int full) { return full / sm_count() * keep; };
     trace_before(kTraceMoeGateup, st);
     if (L.TT == 8) {
         static int g1 = 0;
         if (!g1) g1 = persistent_grid(moe_gateup_kernel<1>);
-        moe_gateup_kernel<1><<<g1, kMoeThreads, 0, st>>>(a);
+        moe_gateup_kernel<1><<<budgeted(g1), kMoeThreads, 0, st>>>(a);
     } else {
         static int g2 = 0;
         if (!g2) g2 = persistent_grid(moe_gateup_kernel<2>);
-        moe_gateup_kernel<2><<<g2, kMoeThreads, 0, st>>>(a);
+        moe_gateup_kernel<2><<<budgeted(g2), kMoeThreads, 0, st>>>(a);
     }
     trace_after(kTraceMoeGateup, st);
     if ((r = launch_status()) != HLA_OK) return r;
@@ -619,19 +701,21 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     if (L.TT == 8) {
         static int d1 = 0;
         if (!d1) d1 = persistent_grid(moe_down_kernel<1>);
-        moe_down_kernel<1><<<d1, kMoeThreads, 0, st>>>(a);
+        moe_down_kernel<1><<<budgeted(d1), kMoeThreads, 0, st>>>(a);
     } else {
         static int d2 = 0;
         if (!d2) d2 = persistent_grid(moe_down_kernel<2>);
-        moe_down_kernel<2><<<d2, kMoeThreads, 0, st>>>(a);
+        moe_down_kernel<2><<<budgeted(d2), kMoeThreads, 0, st>>>(a);
     }
     trace_after(kTraceMoeDown, st);
     if ((r = launch_status()) != HLA_OK) return r;
+    if (shared_side && cudaStreamWaitEvent(st, g_shared_events.join, 0) != cudaSuccess) return HLA_ERR_CUDA;
     const dim3 cgrid((unsigned)((Hd / 4 + 127) / 128), (unsigned)M);
     moe_combine_kernel<<<cgrid, 128, 0, st>>>(a);
     if ((r = launch_status()) != HLA_OK) return r;
     if (side && cudaStreamWaitEvent(st, g_moe_events.join, 0) != cudaSuccess) return HLA_ERR_CUDA;
-    set_variant("moe<tt%d,ks%d,ksd%d%s%s>", L.TT, L.KS, L.KSD, L.shared_tc ? ",shared_tc" : "",
+    set_variant("moe<tt%d,ks%d,ksd%d%s%s>", L.TT, L.KS, L.KSD,
+                L.shared_tc ? ",shared_tc" : (shared_side ? ",shared_side" : ""),
                 side ? ",prefetch" : "");
     return HLA_OK;
 }
@@ -646,13 +730,17 @@ extern "C" size_t moe_expert_forward_workspace_size(int M, int Hd, int I, int E,
     return moe_workspace_bytes(M, Hd, I, E, k, n_shared);
 }
 
-extern "C" int moe_expert_forward(int M, int Hd, int I, int E, int k, int n_shared,
-                                  const hla_bf16 *x, const int32_t *topk_idx, const float *topk_w,
-                                  const hla_bf16 *W_gate, const hla_bf16 *W_up,
-                                  const hla_bf16 *W_down, const hla_bf16 *Ws_gate,
-                                  const hla_bf16 *Ws_up, const hla_bf16 *Ws_down,
-                                  const hla_bf16 *residual, hla_bf16 *y, void *ws,
-                                  size_t ws_bytes, hla_stream stream, hla_stream prefetch_stream) {
+namespace hla {
+
+// Argument checks of moe_expert_forward, then the pipeline.  shared_external: the shared
+// experts were already forked onto the side stream by moe_shared_side (the layer does this
+// before its router).
+int moe_forward_checked(int M, int Hd, int I, int E, int k, int n_shared, const hla_bf16 *x,
+                        const int32_t *topk_idx, const float *topk_w, const hla_bf16 *W_gate,
+                        const hla_bf16 *W_up, const hla_bf16 *W_down, const hla_bf16 *Ws_gate,
+                        const hla_bf16 *Ws_up, const hla_bf16 *Ws_down, const hla_bf16 *residual,
+                        hla_bf16 *y, void *ws, size_t ws_bytes, cudaStream_t st, cudaStream_t pf,
+                        bool shared_external) {
     HLA_REQUIRE(M >= 1 && Hd >= 32 && I >= 32 && E >= 1 && k >= 1 && n_shared >= 0,
                 HLA_ERR_INVALID_ARG);
     HLA_REQUIRE(M <= 256 && k <= 16 && k <= E && E + n_shared <= 1024 && n_shared <= 16 &&
@@ -669,6 +757,19 @@ extern "C" int moe_expert_forward(int M, int Hd, int I, int E, int k, int n_shar
     HLA_REQUIRE(ws && ws_bytes >= need, HLA_ERR_WORKSPACE);
     HLA_REQUIRE(aligned16(ws), HLA_ERR_MISALIGNED);
     return run_moe(M, Hd, I, E, k, n_shared, x, topk_idx, topk_w, W_gate, W_up, W_down, Ws_gate,
-                   Ws_up, Ws_down, residual, y, ws, (cudaStream_t)stream,
-                   (cudaStream_t)prefetch_stream);
+                   Ws_up, Ws_down, residual, y, ws, st, pf, shared_external);
+}
+
+}  // namespace hla
+
+extern "C" int moe_expert_forward(int M, int Hd, int I, int E, int k, int n_shared,
+                                  const hla_bf16 *x, const int32_t *topk_idx, const float *topk_w,
+                                  const hla_bf16 *W_gate, const hla_bf16 *W_up,
+                                  const hla_bf16 *W_down, const hla_bf16 *Ws_gate,
+                                  const hla_bf16 *Ws_up, const hla_bf16 *Ws_down,
+                                  const hla_bf16 *residual, hla_bf16 *y, void *ws,
+                                  size_t ws_bytes, hla_stream stream, hla_stream prefetch_stream) {
+    return moe_forward_checked(M, Hd, I, E, k, n_shared, x, topk_idx, topk_w, W_gate, W_up, W_down,
+                               Ws_gate, Ws_up, Ws_down, residual, y, ws, ws_bytes, (cudaStream_t)stream,
+                               (cudaStream_t)prefetch_stream, false);
 }

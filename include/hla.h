@@ -264,6 +264,12 @@ int moe_route_topk(int M, int Hd, int E, int k, const hla_bf16 *x, const hla_bf1
  *  shared experts' weights runs while routing bookkeeping runs on `stream`;
  *  `stream` joins it before returning, so the call stays capturable as one
  *  graph branch.  Results are bit-identical with and without it.
+ *  With HLA_SHARED_STREAM=1 in the environment the same stream instead runs
+ *  the shared experts as dense SwiGLU products, concurrently with the routed
+ *  experts (the shared expert does not depend on the routing: same page,
+ *  Part 1 sec. 3); `stream` joins it before the final combine.  The shared
+ *  experts' sums then run in another order, so results differ from the
+ *  default placement in the last bits (within the MoE tolerance).
  * -------------------------------------------------------------------------*/
 size_t moe_expert_forward_workspace_size(int M, int Hd, int I, int E, int k, int n_shared);
 int moe_expert_forward(int M, int Hd, int I, int E, int k, int n_shared, const hla_bf16 *x,

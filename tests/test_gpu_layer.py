@@ -105,3 +105,37 @@ def test_layer_in_cuda_graph_matches_eager(dev, layer, M):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(y, y_eager) and torch.equal(S_graph, S_eager)
+
+
+@pytest.mark.parametrize("M", [1, 64])
+def test_layer_shared_experts_on_side_stream(dev, layer, M, monkeypatch):
+    """HLA_SHARED_STREAM=1: the layer forks the shared experts onto its side stream before the
+    router.  The state is untouched by the placement (bit-identical), the output is close to
+    the default placement, and a captured CUDA graph reproduces the eager call bit for bit."""
+    w, L, p = layer
+    x = inputs.activations(M, FULL["Hd"], inputs.generator(4400 + M)).to(dev)
+    S0 = warm_states(4, M, H, D)
+    S_def = S0.to(dev)
+    y_def = _run(dev, L, M, x, S_def, prefetch=True)
+    monkeypatch.setenv("HLA_SHARED_STREAM", "1")
+    S_side = S0.to(dev)
+    y_side = _run(dev, L, M, x, S_side, prefetch=True)
+    torch.cuda.synchronize()
+    assert torch.equal(S_side, S_def)
+    assert frob_rel(f64(y_side), f64(y_def)) < 2e-3
+    y = torch.empty(M, FULL["Hd"], dtype=torch.bfloat16, device=dev)
+    nb = hla.hla_decode_layer_workspace_size(L, M)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream()
+    S_graph = S0.to(dev)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            hla.hla_decode_layer(L, M, x, S_graph, None, y, ws, nb, prefetch_stream=side)
+    S_graph.copy_(S0.to(dev))
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_side) and torch.equal(S_graph, S_side)
+

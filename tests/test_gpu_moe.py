@@ -249,6 +249,38 @@ def test_shared_experts_on_tensor_core_path(dev, M, ks, monkeypatch):
     assert frob_rel(f64(y), y_ref) < MOE_FROB_REL
 
 
+@pytest.mark.parametrize("M", [1, 5, 40])
+def test_shared_experts_on_side_stream(dev, M, monkeypatch):
+    """With HLA_SHARED_STREAM=1 and a side stream, the shared experts run there as dense
+    SwiGLU products (split K, their own partial buffers) while the routed experts run on the
+    main stream; the combine waits for both."""
+    monkeypatch.setenv("HLA_SHARED_STREAM", "1")
+    Hd, I, E, k, ns = 256, 128, 16, 2, 2
+    g = inputs.generator(170 + M)
+    w = inputs.moe_weights(E, Hd, I, ns, g)
+    x, _ = tie_free_activations(M, Hd, f64(w["W_r"]), k, 170 + M)
+    wd = {kk: vv.to(dev) for kk, vv in w.items()}
+    idx_ref, w_ref, _ = oracle.moe.route_topk(f64(x), f64(w["W_r"]), k)
+    idx = torch.from_numpy(idx_ref.astype("int32")).to(dev)
+    wt = torch.from_numpy(w_ref.astype("float32")).to(dev)
+    res = inputs.activations(M, Hd, g).to(dev)
+    y = torch.empty(M, Hd, dtype=torch.bfloat16, device=dev)
+    nb = hla.moe_expert_forward_workspace_size(M, Hd, I, E, k, ns)
+    ws = _ws(nb, dev)
+    side = torch.cuda.Stream()
+    hla.moe_expert_forward(M, Hd, I, E, k, ns, x.to(dev), idx, wt, wd["W_gate"], wd["W_up"],
+                           wd["W_down"], wd["Ws_gate"], wd["Ws_up"], wd["Ws_down"], res, y, ws, nb,
+                           prefetch_stream=side)
+    variant = hla.hla_last_variant()
+    torch.cuda.synchronize()
+    assert "shared_side" in variant, variant
+    shared = [(f64(w["Ws_gate"][s]), f64(w["Ws_up"][s]), f64(w["Ws_down"][s])) for s in range(ns)]
+    y_ref = oracle.moe.moe_forward(f64(x), idx_ref, w_ref,
+                                   (f64(w["W_gate"]), f64(w["W_up"]), f64(w["W_down"])), shared,
+                                   residual=f64(res))
+    assert frob_rel(f64(y), y_ref) < MOE_FROB_REL
+
+
 # ----------------------------------------------------------------------------- full-size MoE
 
 def _run_moe(dev, w, x, idx, wt, residual=None, prefetch=False):
@@ -309,3 +341,31 @@ def test_skewed_routing_and_prefetch_bitwise(dev, full_moe):
     y_ref = oracle.moe.moe_forward(f64(x)[sample], idx.numpy()[sample], f64(wt)[sample], cache,
                                    cache.shared())
     assert frob_rel(f64(y1)[sample], y_ref) < MOE_FROB_REL
+
+
+@pytest.mark.parametrize("M", [1, 8, 64])
+def test_full_moe_shared_on_side_stream(dev, full_moe, M, monkeypatch):
+    """Full-size MoE with the shared expert on the side stream: close to the default placement
+    (grouped work unit; the two differ only in the order of the shared expert's fp32 sums) and
+    within tolerance of the oracle on sampled tokens."""
+    Hd, E, k = FULL["Hd"], FULL["E"], FULL["k"]
+    x, _ = tie_free_activations(M, Hd, full_moe["W_r64"], k, 300 + M)
+    xd = x.to(dev)
+    idx_ref, w_ref, _ = oracle.moe.route_topk(f64(x), full_moe["W_r64"], k)
+    idx = torch.from_numpy(idx_ref.astype("int32")).to(dev)
+    wt = torch.from_numpy(w_ref.astype("float32")).to(dev)
+    res = inputs.activations(M, Hd, inputs.generator(301 + M)).to(dev)
+    y0 = _run_moe(dev, full_moe, xd, idx, wt, residual=res, prefetch=True)
+    monkeypatch.setenv("HLA_SHARED_STREAM", "1")
+    y1 = _run_moe(dev, full_moe, xd, idx, wt, residual=res, prefetch=True)
+    assert "shared_side" in hla.hla_last_variant()
+    y2 = _run_moe(dev, full_moe, xd, idx, wt, residual=res, prefetch=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)                      # deterministic across calls
+    assert frob_rel(f64(y1), f64(y0)) < 2e-3
+    cache = ExpertCache(full_moe)
+    sample = sorted(set([0, M // 2, M - 1]))
+    y_ref = oracle.moe.moe_forward(f64(x)[sample], idx_ref[sample], w_ref[sample], cache,
+                                   cache.shared(), residual=f64(res)[sample])
+    assert frob_rel(f64(y1)[sample], y_ref) < MOE_FROB_REL
+
