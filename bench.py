@@ -557,8 +557,11 @@ def run_ours(args):
 
     # end to end through host buffers: pinned host inputs in, results out, every step.  A step's
     # inputs sit in one pinned buffer and go over in one copy (the library reads them through
-    # views of one device staging buffer); the step's outputs are written into views of one device
-    # buffer and come back in one copy.
+    # views of a device staging buffer); its outputs are written into views of one device buffer
+    # and come back in one copy.  As a serving loop would, the copies run on a second stream,
+    # double-buffered: step i+1's inputs go over and step i-1's outputs come back while step i
+    # computes.  The first copy starts after the timer, and the last read-back is joined before
+    # it stops.
     def packed(tensors):
         """(pinned uint8 host buffer holding the tensors back to back, [(offset, tensor)])."""
         offs, o = [], 0
@@ -578,30 +581,64 @@ def run_ours(args):
     win_keys = list(wl.win[0].keys())
     stage_h, layout = [], None
     for r in range(ROTATE):
-        ts = [wl.x[r]] + [wl.win[r][k2] for k2 in win_keys] + [wl.ids[r][0], wl.ids[r][1]]
-        buf, layout = packed(ts)
+        buf, layout = packed([wl.x[r]] + [wl.win[r][k2] for k2 in win_keys] + [wl.ids[r][0], wl.ids[r][1]])
         stage_h.append(buf)
-    stage_d = torch.empty(stage_h[0].numel(), dtype=torch.uint8, device=dev)
-    views = [view_of(stage_d, off, t) for off, t in layout]
-    xd, wind, dd, td = views[0], dict(zip(win_keys, views[1:1 + len(win_keys)])), views[-2], views[-1]
     out_like = [wl.y, wl.o_spec, wl.acc]
     o_offs, o = [], 0
     for t in out_like:
         o_offs.append(o)
         o += round_up16(t.numel() * t.element_size())
-    out_d = torch.empty(o, dtype=torch.uint8, device=dev)
-    out_h = torch.empty(o, dtype=torch.uint8).pin_memory()
-    wl.y, wl.o_spec, wl.acc = (view_of(out_d, off, t) for off, t in zip(o_offs, out_like))
+    stage_d = [torch.empty(stage_h[0].numel(), dtype=torch.uint8, device=dev) for _ in range(2)]
+    out_d = [torch.empty(o, dtype=torch.uint8, device=dev) for _ in range(2)]
+    out_h = [torch.empty(o, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    in_views = [[view_of(sd, off, t) for off, t in layout] for sd in stage_d]
+    out_views = [[view_of(od, off, t) for off, t in zip(o_offs, out_like)] for od in out_d]
     h2d = stage_h[0].numel()
-    d2h = out_h.numel()
+    d2h = out_h[0].numel()
+    cs = torch.cuda.Stream(device=dev)
+    ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("h2d", "comp", "d2h")}
 
-    def e2e_step(i):
-        r = i % ROTATE
-        stage_d.copy_(stage_h[r], non_blocking=True)
-        wl.step(i, x=xd, win=wind, ids=(dd, td))
-        out_h.copy_(out_d, non_blocking=True)
+    class E2E:
+        """Pipelined end-to-end steps 0..n-1 (call reset(n) before each run)."""
+
+        def reset(self, n):
+            self.n = n
+
+        def __call__(self, i):
+            main = torch.cuda.current_stream()
+            b = i % 2
+            if i == 0:
+                cs.wait_stream(main)
+                with torch.cuda.stream(cs):
+                    stage_d[0].copy_(stage_h[0], non_blocking=True)
+                    ev["h2d"][0].record(cs)
+            if i + 1 < self.n:  # next step's inputs, once step i-1 (same buffer) has computed
+                nb = (i + 1) % 2
+                if i >= 1:
+                    cs.wait_event(ev["comp"][nb])
+                with torch.cuda.stream(cs):
+                    stage_d[nb].copy_(stage_h[(i + 1) % ROTATE], non_blocking=True)
+                    ev["h2d"][nb].record(cs)
+            main.wait_event(ev["h2d"][b])
+            if i >= 2:
+                main.wait_event(ev["d2h"][b])  # step i-2's outputs are back on the host
+            v = in_views[b]
+            wl.y, wl.o_spec, wl.acc = out_views[b]
+            wl.step(i, x=v[0], win=dict(zip(win_keys, v[1:1 + len(win_keys)])), ids=(v[-2], v[-1]))
+            ev["comp"][b].record(main)
+            cs.wait_event(ev["comp"][b])
+            with torch.cuda.stream(cs):
+                out_h[b].copy_(out_d[b], non_blocking=True)
+                ev["d2h"][b].record(cs)
+            if i == self.n - 1:
+                main.wait_stream(cs)
+
+    e2e_step = E2E()
+    e2e_step.reset(2)
     for i in range(2):
         e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_step.reset(args.steps)
     e2e_elapsed = time_steps(torch, e2e_step, args.steps, world, label="e2e")
     e2e_max, _ = reduce_over_ranks(e2e_elapsed, 0, world)
 
