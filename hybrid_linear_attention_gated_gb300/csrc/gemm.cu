@@ -3,10 +3,11 @@
 //
 // "Hyper-optimizing Kimi K3 in vLLM", Part 1 sec. 1: projections at decode batch
 // sizes are skinny products; the pages use small-matrix kernels at batch 1-2 and
-// split-K (K divided over more CTAs, then reduced) above.  Here every projection
-// runs on the warp-level streaming tile (stream_mma.cuh) and the split count is
-// chosen from the problem size so that enough 16-row x K-slice items exist to keep
-// every SM streaming; the second pass sums the fp32 partials in increasing slice
+// split-K (K divided over more CTAs, then reduced) above.  Here, below 32 tokens, every
+// projection runs on the warp-level streaming tile (stream_mma.cuh; a warp item is 32
+// weight rows x one K slice x a group of tokens) with the split count chosen from the
+// problem size so that enough items exist to keep every SM streaming; from 32 tokens the
+// tcgen05 path (tc_gemm.cu) takes over.  Split partials are summed in a fixed slice
 // order, so results are deterministic.
 #include <cstdlib>
 

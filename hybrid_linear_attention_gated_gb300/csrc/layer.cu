@@ -7,7 +7,9 @@
 // projections).  The prefetch stream is passed to the MoE call, which warms the shared
 // expert's rows in L2 during dispatch when several token groups will read them (Part 1
 // sec. 4); warming the output-projection and router weights during the KDA step is
-// available through HLA_PREFETCH_MASK.  All scratch lives in the caller's workspace;
+// available through HLA_PREFETCH_MASK.  With HLA_SHARED_STREAM=1 the shared experts are
+// forked onto the prefetch stream right after the second RMSNorm, so that they overlap the
+// router and dispatch (Part 1 sec. 3).  All scratch lives in the caller's workspace;
 // nothing here allocates or synchronises.
 #include "common.cuh"
 

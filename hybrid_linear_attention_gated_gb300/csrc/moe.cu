@@ -23,6 +23,10 @@
 // Each active expert's weights are read from HBM once per call; when an expert has
 // more than 16 tokens, its token groups are adjacent work items that stream the same
 // rows at the same time, so the repeats are served by L2.
+// The shared experts are, by default, grouped work units 0..n_shared-1 of steps 2-4.  Two
+// opt-in placements compute them instead as dense SwiGLU products into their output slots:
+// on the tensor-core path before dispatch (HLA_SHARED_TC=1, past 16 tokens), or on the side
+// stream concurrently with everything routed (HLA_SHARED_STREAM=1, moe_shared_side).
 #include <cstdlib>
 
 #include "common.cuh"
