@@ -670,7 +670,8 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16 weights/activations, fp32 KDA state and accumulation",
+        "dtype": "bf16",
+        "dtype_note": "bf16 weights and activations with fp32 accumulation; fp32 KDA state and arithmetic",
         "data": "synthetic (seeded; random-init weights of the layer's shapes)",
         "config": {
             "workload": "hybrid decode layer at batch 64 (hidden 7168; KDA 32 heads x 128, fp32 "
