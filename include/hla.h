@@ -73,7 +73,7 @@ enum hla_spec_phase { HLA_SPEC_VERIFY = 1, HLA_SPEC_REPLAY = 2 };
 const char *hla_status_string(int status);
 
 /* Name of the kernel variant the calling thread's most recent entry point
- * launched (e.g. "kda_recur<128,cw16,decode>"), for tests that must prove which
+ * launched (e.g. "kda_recur<dk128,cw16,decode>"), for tests that must prove which
  * path ran.  Static/thread-local storage; "" before the first call. */
 const char *hla_last_variant(void);
 
@@ -202,9 +202,10 @@ int skinny_proj_splitk(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W
  *  r  = residual + x W^T            stored bf16 [M, N]   (residual bf16 [M, N] or NULL)
  *  xn = r * gamma / sqrt(mean(r^2) + eps)   over each row, stored bf16 [M, N]
  *  x bf16 [M, K]; W bf16 [N, K]; gamma bf16 [N]; K % 32 == 0, N % 8 == 0, 1 <= M <= 256.
- *  split as skinny_proj_splitk (0 = automatic).  Bit-identical to skinny_proj_splitk (bf16
- *  output) followed by hla_rmsnorm with the same split.  The workspace holds the fp32
- *  split partials (at least one slice).
+ *  split as skinny_proj_splitk (0 = automatic; below 32 tokens the automatic split is at
+ *  most 8, since the normalising pass sums every slice of a row in one CTA).  Bit-identical
+ *  to skinny_proj_splitk (bf16 output) followed by hla_rmsnorm with the same split.  The
+ *  workspace holds the fp32 split partials (at least one slice).
  * -------------------------------------------------------------------------*/
 size_t skinny_proj_residual_rmsnorm_workspace_size(int M, int N, int K, int split);
 int skinny_proj_residual_rmsnorm(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W,
@@ -309,7 +310,9 @@ typedef struct hla_layer {
 
 /*  M sequences (one token each, 1 <= M <= 256); x, y bf16 [M, Hd] (distinct);
  *  S fp32 [n_slots, H, dk, dv] in place; state_idx as kda_decode_step.
- *  prefetch_stream as moe_expert_forward (NULL = no prefetch). */
+ *  prefetch_stream as moe_expert_forward (NULL = no prefetch); with HLA_SHARED_STREAM=1
+ *  the shared experts are forked onto it right after the second RMSNorm, before the router.
+ *  All scratch is in ws (hla_decode_layer_workspace_size bytes, 16-byte aligned). */
 size_t hla_decode_layer_workspace_size(const hla_layer *L, int M);
 int hla_decode_layer(const hla_layer *L, int M, const hla_bf16 *x, float *S,
                      const int32_t *state_idx, hla_bf16 *y, void *ws, size_t ws_bytes,
