@@ -298,12 +298,15 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t K, uin
 
 template <int MT>
 int launch_tc(const TcParams &p, const void *W, const void *x, cudaStream_t st) {
-    static bool attr_done = false;
-    if (!attr_done) {
+    // the shared-memory limit is a per-device attribute: raise it once on every device used
+    static bool attr_done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return HLA_ERR_CUDA;
+    if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(dense_tc_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)tc_smem_bytes<MT>()) != cudaSuccess)
             return HLA_ERR_CUDA;
-        attr_done = true;
+        attr_done[dev] = true;
     }
     CUtensorMap mw, mx;
     if (!make_map(&mw, W, p.N, p.K, kRows) || !make_map(&mx, x, p.M, p.K, MT)) return HLA_ERR_CUDA;
