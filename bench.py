@@ -727,9 +727,9 @@ def run_profile(kind, iters=3):
     g = inputs.generator(500, dev)
     info = dict(case=kind)
     if kind == "moe":
-        # 48 experts, 16 tokens, top-8: ~2.6 tokens per active expert (as at batch 64 with
-        # 256 experts) and the same 16-token tile variant as the full workload
-        E, M = 48, 16
+        # 48 experts, 32 tokens, top-8: the same kernel variants as the batch-64 workload
+        # (16-token tile, the 2-step gate/up pipeline used from 32 tokens), 4.2 GB of weights
+        E, M = 48, 32
         w = inputs.moe_weights(E, c["Hd"], c["I"], c["n_shared"], g, device=dev)
         x = inputs.activations(M, c["Hd"], g, dev)
         idx = torch.empty(M, c["k"], dtype=torch.int32, device=dev)

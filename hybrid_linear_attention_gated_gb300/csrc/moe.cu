@@ -79,6 +79,12 @@ int moe_tokens_per_tile(int M) { return M <= 8 ? 8 : 16; }
 //    claimed end soon after the others (at batch 8: 726 us with splits 4 / 2 against 775 us
 //    unsplit; at batch 32 and 64 splitting measured no better or slower, the partials then
 //    being large).
+// HLA_MOE_SHALLOW=0 keeps the 4-step gate/up pipeline at every batch (A/B measurements).
+bool moe_shallow_gateup() {
+    const char *env = getenv("HLA_MOE_SHALLOW");
+    return !(env && env[0] == '0');
+}
+
 int moe_items_split(int M, int k, int E, int nsh, long row_blocks, long cap) {
     long units = (long)M * k < E ? (long)M * k : E;
     units += nsh;
@@ -297,7 +303,7 @@ __device__ __forceinline__ int find_unit(const int *pref, int U, int it) {
     return lo;
 }
 
-template <int NT>
+template <int NT, int UNROLL>
 __global__ void __launch_bounds__(kMoeThreads) moe_gateup_kernel(const MoeArgs a) {
     const int U = a.meta[0];
     const int total = a.item_gu[U];
@@ -334,7 +340,7 @@ __global__ void __launch_bounds__(kMoeThreads) moe_gateup_kernel(const MoeArgs a
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) acc[m][nt][q] = 0.f;
-        warp_stream_tile<2, NT, 4>(wg, wg8, xr, kb, ke, acc);
+        warp_stream_tile<2, NT, UNROLL>(wg, wg8, xr, kb, ke, acc);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -686,14 +692,24 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     const int keep = shared_side ? sm_count() - shared_sm_budget() : sm_count();
     auto budgeted = [&](int full) { return full / sm_count() * keep; };
     trace_before(kTraceMoeGateup, st);
+    // K steps of loads in flight per warp in the gate/up kernel: 4, or 2 from 32 tokens (fewer
+    // registers, 4 resident CTAs per SM instead of 3).  Measured on the decode layer (CUDA
+    // graph, same box): with 2, gate/up at batch 64 took 1910 us against 1958 and the layer
+    // 3075 us against 3100, batch 32 2224 us against 2283; at batch 16 it was slower (1940 us
+    // against 1609), and the down kernel did not gain.
+    const bool shallow = L.TT == 16 && M >= 32 && moe_shallow_gateup();
     if (L.TT == 8) {
         static int g1 = 0;
-        if (!g1) g1 = persistent_grid(moe_gateup_kernel<1>);
-        moe_gateup_kernel<1><<<budgeted(g1), kMoeThreads, 0, st>>>(a);
+        if (!g1) g1 = persistent_grid(moe_gateup_kernel<1, 4>);
+        moe_gateup_kernel<1, 4><<<budgeted(g1), kMoeThreads, 0, st>>>(a);
+    } else if (shallow) {
+        static int g3 = 0;
+        if (!g3) g3 = persistent_grid(moe_gateup_kernel<2, 2>);
+        moe_gateup_kernel<2, 2><<<budgeted(g3), kMoeThreads, 0, st>>>(a);
     } else {
         static int g2 = 0;
-        if (!g2) g2 = persistent_grid(moe_gateup_kernel<2>);
-        moe_gateup_kernel<2><<<budgeted(g2), kMoeThreads, 0, st>>>(a);
+        if (!g2) g2 = persistent_grid(moe_gateup_kernel<2, 4>);
+        moe_gateup_kernel<2, 4><<<budgeted(g2), kMoeThreads, 0, st>>>(a);
     }
     trace_after(kTraceMoeGateup, st);
     if ((r = launch_status()) != HLA_OK) return r;
@@ -718,7 +734,7 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     moe_combine_kernel<<<cgrid, 128, 0, st>>>(a);
     if ((r = launch_status()) != HLA_OK) return r;
     if (side && cudaStreamWaitEvent(st, g_moe_events.join, 0) != cudaSuccess) return HLA_ERR_CUDA;
-    set_variant("moe<tt%d,ks%d,ksd%d%s%s>", L.TT, L.KS, L.KSD,
+    set_variant("moe<tt%d,ks%d,ksd%d%s%s%s>", L.TT, L.KS, L.KSD, shallow ? ",u2" : "",
                 L.shared_tc ? ",shared_tc" : (shared_side ? ",shared_side" : ""),
                 side ? ",prefetch" : "");
     return HLA_OK;
