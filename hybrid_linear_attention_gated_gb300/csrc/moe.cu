@@ -85,6 +85,25 @@ bool moe_shallow_gateup() {
     return !(env && env[0] == '0');
 }
 
+// HLA_MOE_XITEM=0 keeps the expert kernels whose loads stop at item boundaries (A/B runs).
+bool moe_cross_item() {
+    const char *env = getenv("HLA_MOE_XITEM");
+    return !(env && env[0] == '0');
+}
+
+// Fewest K steps of 32 in any of the `split` slices of [0, K) that k_slice hands out.
+int min_slice_steps(int K, int split) {
+    const int steps = K >> 5;
+    const int per = (steps + split - 1) / split;
+    int mn = steps;
+    for (int s = 0; s < split; ++s) {
+        const int kb = s * per < steps ? s * per : steps;
+        const int ke = (s + 1) * per < steps ? (s + 1) * per : steps;
+        if (ke - kb < mn) mn = ke - kb;
+    }
+    return mn;
+}
+
 int moe_items_split(int M, int k, int E, int nsh, long row_blocks, long cap) {
     long units = (long)M * k < E ? (long)M * k : E;
     units += nsh;
@@ -433,6 +452,230 @@ __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(const MoeArgs a) 
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Cross-item pipeline.  In the two kernels above a warp's loads stop at the end of every
+// work item: its ring drains, the next item is claimed and decoded, and only then are that
+// item's first loads issued, so each item boundary leaves the warp with nothing in flight
+// for about one atomic plus one memory latency.  With items of 64-128 KB of weights (the
+// down projection, and both products at small batch) that gap is a visible share of an
+// item.  stream_items keeps the ring of UNROLL K steps running across item boundaries: the
+// next item is claimed kClaimAhead steps before its first loads are due (late, so that the
+// dynamic balance between warps stays as it was: at batch 1 a warp has about two items)
+// and decoded just before them, and the last steps of one item are multiplied while the
+// first loads of the next are already in flight.  Every item must have at least UNROLL K
+// steps (the host checks the K slices), so the loads ahead reach at most into the next item.
+constexpr int kClaimAhead = 2;
+
+// lane 0 claims; the index is broadcast when it is used, a few steps later
+__device__ __forceinline__ int claim_lane0(int *counter) {
+    return (threadIdx.x & 31) == 0 ? atomicAdd(counter, 1) : 0;
+}
+
+// What a warp streams for one work item: weight row g of each matrix (row g + 8 lies ld8
+// elements further on) and the token row of each 8-token tile, all offset to the item's
+// first K value; n K steps of 32 (0: no item); ctx is what the item's epilogue needs.
+template <int NMAT, int NT, class Ctx>
+struct ItemRows {
+    const uint16_t *w[NMAT];
+    const uint16_t *x[NT];
+    int n;
+    Ctx ctx;
+    __device__ __forceinline__ void load(int s, size_t ld8, uint4 (&wa)[NMAT][2],
+                                         uint4 (&xb)[NT]) const {
+        const int k = 32 * s + (threadIdx.x & 3) * 8;
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+            wa[m][0] = ld_weight_v4(w[m] + k);
+            wa[m][1] = ld_weight_v4(w[m] + ld8 + k);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) xb[nt] = ld_act_v4(x[nt] + k);
+    }
+};
+
+template <int NMAT, int NT>
+__device__ __forceinline__ void zero_acc(float (&acc)[NMAT][NT][4]) {
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[m][nt][q] = 0.f;
+}
+
+// decode(it) -> ItemRows of work item it (< total); epilogue(ctx, acc) stores an item's result.
+template <int NMAT, int NT, int UNROLL, class Ctx, class Decode, class Epilogue>
+__device__ __forceinline__ void stream_items(int *counter, int total, size_t ld8,
+                                             const Decode &decode, const Epilogue &epilogue) {
+    using Item = ItemRows<NMAT, NT, Ctx>;
+    int it = claim_item(counter);
+    if (it >= total) return;
+    Item cur = decode(it);
+    Item nxt;
+    nxt.n = 0;
+    int pend = 0;
+    uint4 wa[UNROLL][NMAT][2];
+    uint4 xb[UNROLL][NT];
+    float acc[NMAT][NT][4];
+    zero_acc<NMAT, NT>(acc);
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) cur.load(u, ld8, wa[u], xb[u]);
+    int ls = 0;  // the step of cur that ring slot u holds
+    for (;;) {
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int first_next = cur.n - UNROLL;  // the step whose refill is next's step 0
+            if (ls == (first_next > kClaimAhead ? first_next - kClaimAhead : 0))
+                pend = claim_lane0(counter);
+            mma_step<NMAT, NT>(wa[u], xb[u], acc);
+            if (ls == first_next) {
+                it = __shfl_sync(0xffffffffu, pend, 0);
+                if (it < total) nxt = decode(it);
+            }
+            int j = ls + UNROLL;  // the step that refills slot u, counted from cur's first
+            if (ls == cur.n - 1) {
+                epilogue(cur.ctx, acc);
+                zero_acc<NMAT, NT>(acc);
+                if (nxt.n == 0) return;
+                cur = nxt;
+                nxt.n = 0;
+                ls = -1;
+                j = UNROLL - 1;
+            }
+            if (j < cur.n) cur.load(j, ld8, wa[u], xb[u]);
+            else if (j - cur.n < nxt.n) nxt.load(j - cur.n, ld8, wa[u], xb[u]);
+            ++ls;
+        }
+    }
+}
+
+struct GateupCtx {
+    int pt, p1, ks, rb;  // first position of the token group, end of the unit, K slice, row block
+};
+
+// Resident CTAs per SM the cross-item kernels keep (at most 65536 / (128 x 128) registers
+// each for 4): the same residency as the kernels without the cross-item ring.
+constexpr int xi_min_blocks(int NT, int UNROLL) { return (NT == 1 || UNROLL == 2) ? 4 : 3; }
+
+template <int NT, int UNROLL>
+__global__ void __launch_bounds__(kMoeThreads, xi_min_blocks(NT, UNROLL))
+    moe_gateup_xi_kernel(const MoeArgs a) {
+    const int U = a.meta[0];
+    const int total = a.item_gu[U];
+    const int g = (threadIdx.x & 31) >> 2;
+    auto decode = [&](int it) {
+        ItemRows<2, NT, GateupCtx> r;
+        const int u = find_unit(a.item_gu, U, it);
+        const int local = it - a.item_gu[u];
+        const int p0 = a.unit_off[u], p1 = a.unit_off[u + 1];
+        const int ntg = (p1 - p0 + a.TT - 1) / a.TT;
+        const int tg = local % ntg;
+        const int rest = local / ntg;
+        const int ks = rest % a.KS;
+        const int rb = rest / a.KS;
+        const int e = a.unit_expert[u];
+        int kb, ke;
+        k_slice(a.Hd, a.KS, ks, kb, ke);
+        // I is a multiple of 32, so rows rb*16 + g + 8 never pass the last row
+        const size_t roff = (size_t)(e < a.E ? e : e - a.E) * a.I * a.Hd +
+                            (size_t)(rb * 16 + g) * a.Hd + kb;
+        r.w[0] = (e < a.E ? a.W_gate : a.Ws_gate) + roff;
+        r.w[1] = (e < a.E ? a.W_up : a.Ws_up) + roff;
+        const int pt = p0 + tg * a.TT;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int p = pt + nt * 8 + g;
+            r.x[nt] = a.x + (size_t)a.pos_token[p < p1 ? p : pt] * a.Hd + kb;
+        }
+        r.n = (ke - kb) >> 5;
+        r.ctx = GateupCtx{pt, p1, ks, rb};
+        return r;
+    };
+    auto epilogue = [&](const GateupCtx &c, float (&acc)[2][NT][4]) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int row = c.rb * 16 + acc_row(q);
+                const int p = c.pt + acc_tok(nt, q);
+                if (p >= c.p1) continue;
+                if (a.KS == 1) {
+                    a.h[(size_t)p * a.I + row] =
+                        float_to_bf16_bits(__fmul_rn(silu_f(acc[0][nt][q]), acc[1][nt][q]));
+                } else {
+                    const size_t o = ((size_t)c.ks * a.P + p) * a.I + row;
+                    a.part_g[o] = acc[0][nt][q];
+                    a.part_u[o] = acc[1][nt][q];
+                }
+            }
+        }
+    };
+    stream_items<2, NT, UNROLL, GateupCtx>(&a.meta[3], total, (size_t)8 * a.Hd, decode, epilogue);
+}
+
+template <int NT>
+struct DownCtx {
+    int ks, rbase;     // K slice, first of the item's 32 rows
+    int slot[NT][2];   // output slot of the two tokens this lane holds in tile nt (-1: none)
+};
+
+template <int NT>
+__global__ void __launch_bounds__(kMoeThreads, xi_min_blocks(NT, 4)) moe_down_xi_kernel(const MoeArgs a) {
+    const int U = a.meta[0];
+    const int total = a.item_dn[U];
+    const int g = (threadIdx.x & 31) >> 2;
+    const int t2 = (threadIdx.x & 3) * 2;
+    auto decode = [&](int it) {
+        ItemRows<2, NT, DownCtx<NT>> r;
+        const int u = find_unit(a.item_dn, U, it);
+        const int local = it - a.item_dn[u];
+        const int p0 = a.unit_off[u], p1 = a.unit_off[u + 1];
+        const int ntg = (p1 - p0 + a.TT - 1) / a.TT;
+        const int tg = local % ntg;
+        const int ks = (local / ntg) % a.KSD;
+        const int rbase = local / ntg / a.KSD * 32;
+        const int e = a.unit_expert[u];
+        int kb, ke;
+        k_slice(a.I, a.KSD, ks, kb, ke);
+        // Hd is a multiple of 32, so rows rbase + 24 + g never pass the last row
+        const uint16_t *Wd = (e < a.E ? a.W_down : a.Ws_down) +
+                             (size_t)(e < a.E ? e : e - a.E) * a.Hd * a.I + kb;
+        r.w[0] = Wd + (size_t)(rbase + g) * a.I;
+        r.w[1] = Wd + (size_t)(rbase + 16 + g) * a.I;
+        const int pt = p0 + tg * a.TT;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int p = pt + nt * 8 + g;
+            r.x[nt] = a.h + (size_t)(p < p1 ? p : pt) * a.I + kb;
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int q = pt + nt * 8 + t2 + e2;
+                r.ctx.slot[nt][e2] = q < p1 ? a.pos_slot[q] : -1;
+            }
+        }
+        r.n = (ke - kb) >> 5;
+        r.ctx.ks = ks;
+        r.ctx.rbase = rbase;
+        return r;
+    };
+    auto epilogue = [&](const DownCtx<NT> &c, float (&acc)[2][NT][4]) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int slot = c.slot[nt][q & 1];
+                    if (slot < 0) continue;
+                    const int row = c.rbase + 16 * h + acc_row(q);
+                    a.ypart[((size_t)c.ks * a.P + slot) * a.Hd + row] = acc[h][nt][q];
+                }
+            }
+        }
+    };
+    stream_items<2, NT, 4, DownCtx<NT>>(&a.meta[4], total, (size_t)8 * a.I, decode, epilogue);
+}
+
 // y[m] = sum_j w[m,j] * (sum over down slices of y[m,j]) (+ residual): slots in increasing
 // order, slices in increasing order.  Slots are taken four at a time with their routing
 // entries and all their slice rows loaded before any of them is used, so each group of four
@@ -698,18 +941,39 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     // 3075 us against 3100, batch 32 2224 us against 2283; at batch 16 it was slower (1940 us
     // against 1609), and the down kernel did not gain.
     const bool shallow = L.TT == 16 && M >= 32 && moe_shallow_gateup();
+    // The cross-item kernels need every K slice to hold at least the ring's depth in steps.
+    const bool xgu = moe_cross_item() && min_slice_steps(Hd, L.KS) >= (shallow ? 2 : 4);
+    const bool xdn = moe_cross_item() && min_slice_steps(I, L.KSD) >= 4;
     if (L.TT == 8) {
-        static int g1 = 0;
-        if (!g1) g1 = persistent_grid(moe_gateup_kernel<1, 4>);
-        moe_gateup_kernel<1, 4><<<budgeted(g1), kMoeThreads, 0, st>>>(a);
+        if (xgu) {
+            static int g = 0;
+            if (!g) g = persistent_grid(moe_gateup_xi_kernel<1, 4>);
+            moe_gateup_xi_kernel<1, 4><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+        } else {
+            static int g = 0;
+            if (!g) g = persistent_grid(moe_gateup_kernel<1, 4>);
+            moe_gateup_kernel<1, 4><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+        }
     } else if (shallow) {
-        static int g3 = 0;
-        if (!g3) g3 = persistent_grid(moe_gateup_kernel<2, 2>);
-        moe_gateup_kernel<2, 2><<<budgeted(g3), kMoeThreads, 0, st>>>(a);
+        if (xgu) {
+            static int g = 0;
+            if (!g) g = persistent_grid(moe_gateup_xi_kernel<2, 2>);
+            moe_gateup_xi_kernel<2, 2><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+        } else {
+            static int g = 0;
+            if (!g) g = persistent_grid(moe_gateup_kernel<2, 2>);
+            moe_gateup_kernel<2, 2><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+        }
     } else {
-        static int g2 = 0;
-        if (!g2) g2 = persistent_grid(moe_gateup_kernel<2, 4>);
-        moe_gateup_kernel<2, 4><<<budgeted(g2), kMoeThreads, 0, st>>>(a);
+        if (xgu) {
+            static int g = 0;
+            if (!g) g = persistent_grid(moe_gateup_xi_kernel<2, 4>);
+            moe_gateup_xi_kernel<2, 4><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+        } else {
+            static int g = 0;
+            if (!g) g = persistent_grid(moe_gateup_kernel<2, 4>);
+            moe_gateup_kernel<2, 4><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+        }
     }
     trace_after(kTraceMoeGateup, st);
     if ((r = launch_status()) != HLA_OK) return r;
@@ -719,13 +983,25 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     }
     trace_before(kTraceMoeDown, st);
     if (L.TT == 8) {
-        static int d1 = 0;
-        if (!d1) d1 = persistent_grid(moe_down_kernel<1>);
-        moe_down_kernel<1><<<budgeted(d1), kMoeThreads, 0, st>>>(a);
+        if (xdn) {
+            static int d = 0;
+            if (!d) d = persistent_grid(moe_down_xi_kernel<1>);
+            moe_down_xi_kernel<1><<<budgeted(d), kMoeThreads, 0, st>>>(a);
+        } else {
+            static int d = 0;
+            if (!d) d = persistent_grid(moe_down_kernel<1>);
+            moe_down_kernel<1><<<budgeted(d), kMoeThreads, 0, st>>>(a);
+        }
     } else {
-        static int d2 = 0;
-        if (!d2) d2 = persistent_grid(moe_down_kernel<2>);
-        moe_down_kernel<2><<<budgeted(d2), kMoeThreads, 0, st>>>(a);
+        if (xdn) {
+            static int d = 0;
+            if (!d) d = persistent_grid(moe_down_xi_kernel<2>);
+            moe_down_xi_kernel<2><<<budgeted(d), kMoeThreads, 0, st>>>(a);
+        } else {
+            static int d = 0;
+            if (!d) d = persistent_grid(moe_down_kernel<2>);
+            moe_down_kernel<2><<<budgeted(d), kMoeThreads, 0, st>>>(a);
+        }
     }
     trace_after(kTraceMoeDown, st);
     if ((r = launch_status()) != HLA_OK) return r;
@@ -734,7 +1010,8 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     moe_combine_kernel<<<cgrid, 128, 0, st>>>(a);
     if ((r = launch_status()) != HLA_OK) return r;
     if (side && cudaStreamWaitEvent(st, g_moe_events.join, 0) != cudaSuccess) return HLA_ERR_CUDA;
-    set_variant("moe<tt%d,ks%d,ksd%d%s%s%s>", L.TT, L.KS, L.KSD, shallow ? ",u2" : "",
+    set_variant("moe<tt%d,ks%d,ksd%d%s%s%s%s%s>", L.TT, L.KS, L.KSD, shallow ? ",u2" : "",
+                xgu ? ",xgu" : "", xdn ? ",xdn" : "",
                 L.shared_tc ? ",shared_tc" : (shared_side ? ",shared_side" : ""),
                 side ? ",prefetch" : "");
     return HLA_OK;

@@ -21,6 +21,23 @@
 
 namespace hla {
 
+// One K step (32 values) for one warp: acc[m][nt] += W_m[16 rows] . X[8 tokens of tile nt]^T
+// from the fragments this lane loaded (wa[m][0] / wa[m][1]: rows g / g+8; xb[nt]: its token row).
+template <int NMAT, int NT>
+__device__ __forceinline__ void mma_step(const uint4 (&wa)[NMAT][2], const uint4 (&xb)[NT],
+                                         float (&acc)[NMAT][NT][4]) {
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            mma_bf16_16816(acc[m][nt], wa[m][0].x, wa[m][1].x, wa[m][0].y, wa[m][1].y, xb[nt].x,
+                           xb[nt].y);
+            mma_bf16_16816(acc[m][nt], wa[m][0].z, wa[m][1].z, wa[m][0].w, wa[m][1].w, xb[nt].z,
+                           xb[nt].w);
+        }
+    }
+}
+
 // Accumulate, for one warp, acc[m][nt] += W_m[16 rows] . X[8 tokens of tile nt]^T over
 // K in [kb, ke) (multiples of 32).  wg[m] / wg8[m] point at weight rows g and g+8 of
 // matrix m (element 0 of the row); xr[nt] points at the token row that lane group g
@@ -55,16 +72,7 @@ __device__ __forceinline__ void warp_stream_tile(const uint16_t *const (&wg)[NMA
         for (int u = 0; u < UNROLL; ++u) {
             const int s = s0 + u;
             if (s < nsteps) {
-#pragma unroll
-                for (int m = 0; m < NMAT; ++m) {
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        mma_bf16_16816(acc[m][nt], wa[u][m][0].x, wa[u][m][1].x, wa[u][m][0].y,
-                                       wa[u][m][1].y, xb[u][nt].x, xb[u][nt].y);
-                        mma_bf16_16816(acc[m][nt], wa[u][m][0].z, wa[u][m][1].z, wa[u][m][0].w,
-                                       wa[u][m][1].w, xb[u][nt].z, xb[u][nt].w);
-                    }
-                }
+                mma_step<NMAT, NT>(wa[u], xb[u], acc);
                 if (s + UNROLL < nsteps) {
                     const int k = kb + 32 * (s + UNROLL) + t8;
 #pragma unroll

@@ -369,3 +369,58 @@ def test_full_moe_shared_on_side_stream(dev, full_moe, M, monkeypatch):
                                    cache.shared(), residual=f64(res)[sample])
     assert frob_rel(f64(y1)[sample], y_ref) < MOE_FROB_REL
 
+
+
+# ----------------------------------------------------------------------------- cross-item pipeline
+
+def _skewed_routing(M, E, k, seed):
+    """Distinct top-k experts per token drawn with weights 1/(e+1), so the first experts collect
+    many tokens (several token groups) and the last few, one or none; normalised positive weights."""
+    rng = np.random.default_rng(seed)
+    p = 1.0 / np.arange(1, E + 1)
+    p /= p.sum()
+    idx = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(M)]).astype(np.int32)
+    raw = rng.random((M, k)) + 0.1
+    return idx, raw / raw.sum(1, keepdims=True)
+
+
+@pytest.mark.parametrize("M,ks,ksd", [(3, "1", "1"), (3, "2", "2"), (12, "1", "1"), (12, "3", "2"),
+                                      (40, "1", "1"), (40, "2", "2"), (64, "3", "1")])
+def test_cross_item_pipeline_bitwise(dev, M, ks, ksd, monkeypatch):
+    """The expert kernels whose load ring runs across work-item boundaries give the same bits
+    as the kernels whose loads stop at each item (same products, same summation order), and
+    match the oracle.  Hidden 544 (17 K steps) and intermediate 320 (10 K steps) with forced
+    K splits make item lengths that are not multiples of the ring depth, so the ring's phase
+    moves at every boundary; 8- and 16-token tiles, the 2-step gate/up ring from 32 tokens."""
+    Hd, I, E, k, ns = 544, 320, 16, 4, 1
+    monkeypatch.setenv("HLA_MOE_SPLIT", ks)
+    monkeypatch.setenv("HLA_MOE_DOWN_SPLIT", ksd)
+    g = inputs.generator(600 + M)
+    w = inputs.moe_weights(E, Hd, I, ns, g)
+    x = inputs.activations(M, Hd, g)
+    res = inputs.activations(M, Hd, g)
+    idx_np, wt_np = _skewed_routing(M, E, k, 600 + M)
+    wd = {kk: vv.to(dev) for kk, vv in w.items()}
+    xd, rd = x.to(dev), res.to(dev)
+    idx = torch.from_numpy(idx_np).to(dev)
+    wt = torch.from_numpy(wt_np.astype(np.float32)).to(dev)
+    nb = hla.moe_expert_forward_workspace_size(M, Hd, I, E, k, ns)
+    ws = _ws(nb, dev)
+    out = {}
+    for xi in ("1", "0"):
+        monkeypatch.setenv("HLA_MOE_XITEM", xi)
+        y = torch.empty(M, Hd, dtype=torch.bfloat16, device=dev)
+        hla.moe_expert_forward(M, Hd, I, E, k, ns, xd, idx, wt, wd["W_gate"], wd["W_up"],
+                               wd["W_down"], wd["Ws_gate"], wd["Ws_up"], wd["Ws_down"], rd, y, ws, nb)
+        out[xi] = (y, hla.hla_last_variant())
+    torch.cuda.synchronize()
+    assert hla.hla_device_status() == 0
+    v1, v0 = out["1"][1], out["0"][1]
+    assert ",xgu" in v1 and ",xdn" in v1 and f"ks{ks}," in v1 and f"ksd{ksd}" in v1, v1
+    assert ",xgu" not in v0 and ",xdn" not in v0, v0
+    assert torch.equal(out["1"][0], out["0"][0])
+    shared = [(f64(w["Ws_gate"][0]), f64(w["Ws_up"][0]), f64(w["Ws_down"][0]))]
+    y_ref = oracle.moe.moe_forward(f64(x), idx_np, wt_np.astype(np.float64),
+                                   (f64(w["W_gate"]), f64(w["W_up"]), f64(w["W_down"])), shared,
+                                   residual=f64(res))
+    assert frob_rel(f64(out["1"][0]), y_ref) < MOE_FROB_REL
