@@ -755,8 +755,9 @@ def run_profile(kind, iters=3):
         for _ in range(iters):
             hla.kda_decode_step(B, H, d, d, S, None, u["q"], u["k"], u["v"], u["alpha"], u["beta"], o)
         info.update(B=B, bytes=kda_bytes(B), variant=hla.hla_last_variant())
-    elif kind == "dense":
-        M, H, d = 64, c["H"], c["d"]
+    elif kind in ("dense", "dense16"):
+        # the input projection at batch 64 (tensor-core path) or 16 (streaming path)
+        M, H, d = (64 if kind == "dense" else 16), c["H"], c["d"]
         W = inputs.weight((4 * H * d + H, c["Hd"]), g, dev)
         x = inputs.activations(M, c["Hd"], g, dev)
         outs = [torch.empty(M, H, d, dtype=torch.bfloat16, device=dev) for _ in range(3)]
@@ -897,7 +898,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true")
-    ap.add_argument("--profile", choices=["moe", "kda", "dense"],
+    ap.add_argument("--profile", choices=["moe", "kda", "dense", "dense16"],
                     help="run one small case of a hot kernel (for ncu captures) and exit")
     ap.add_argument("--prefetch-ab", action="store_true",
                     help="time the layer under every side-stream prefetch mask and exit")

@@ -94,6 +94,69 @@ __global__ void __launch_bounds__(kDenseThreads) dense_stream_kernel(const Dense
     }
 }
 
+// The same items on persistent warps whose load ring runs across item boundaries
+// (stream_items): warp w of nwarps takes items w, w + nwarps, ...; the host picks nwarps so
+// that every warp gets the same number of items.  Needs N a multiple of 32 (rows g + 8 of a
+// tile never pass the last row) and every K slice at least 4 steps long.
+struct DenseCtx {
+    int rbase, ks, m0;  // first of the item's 32 rows, K slice, first token of its group
+};
+
+constexpr int dense_xi_min_blocks(int NT) { return NT == 1 ? 4 : 3; }
+
+template <int NT>
+__global__ void __launch_bounds__(kDenseThreads, dense_xi_min_blocks(NT))
+    dense_stream_xi_kernel(const DenseParams p, int nwarps) {
+    const int warp = (blockIdx.x * kDenseThreads + threadIdx.x) >> 5;
+    if (warp >= nwarps) return;  // whole warp leaves together
+    const int total = (p.N >> 5) * p.split * p.ntg;
+    const int g = (threadIdx.x & 31) >> 2;
+    auto decode = [&](int item) {
+        ItemRows<2, NT, DenseCtx> r;
+        const int tg = item % p.ntg;
+        const int rest = item / p.ntg;
+        const int ks = rest % p.split;
+        const int rbase = rest / p.split * 32;
+        int kb, ke;
+        k_slice(p.K, p.split, ks, kb, ke);
+        r.w[0] = p.W + (size_t)(rbase + g) * p.K + kb;
+        r.w[1] = p.W + (size_t)(rbase + 16 + g) * p.K + kb;
+        const int m0 = tg * 8 * NT;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) r.x[nt] = p.x + (size_t)min(m0 + nt * 8 + g, p.M - 1) * p.K + kb;
+        r.n = (ke - kb) >> 5;
+        r.ctx = DenseCtx{rbase, ks, m0};
+        return r;
+    };
+    auto epilogue = [&](const DenseCtx &c, float (&acc)[2][NT][4]) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = c.rbase + 16 * h + acc_row(e);
+                    const int m = c.m0 + acc_tok(nt, e);
+                    if (m >= p.M) continue;
+                    const size_t o = (size_t)m * p.N + r;
+                    if (p.part) {
+                        p.part[(size_t)c.ks * p.M * p.N + o] = acc[h][nt][e];
+                    } else {
+                        float v = acc[h][nt][e];
+                        if (p.residual) v = __fadd_rn(v, bf16_bits_to_float(p.residual[o]));
+                        if (p.y_bf16)
+                            reinterpret_cast<uint16_t *>(p.y)[o] = float_to_bf16_bits(v);
+                        else
+                            reinterpret_cast<float *>(p.y)[o] = v;
+                    }
+                }
+            }
+        }
+    };
+    StridedClaims claims{warp, nwarps};
+    stream_items<2, NT, 4, DenseCtx>(claims, total, (size_t)8 * p.K, decode, epilogue);
+}
+
 // y = sum over slices in increasing order (+ residual)
 __global__ void splitk_reduce_kernel(const float *__restrict__ part, int split, int M, int N,
                                      const uint16_t *__restrict__ residual, void *y, int y_bf16) {
@@ -408,12 +471,41 @@ __global__ void l2_prefetch_kernel(const char *p, size_t bytes, uint32_t chunk) 
     }
 }
 
+// HLA_DENSE_XITEM=0 keeps one item per warp on the streaming path (A/B runs).
+bool dense_cross_item() {
+    const char *env = getenv("HLA_DENSE_XITEM");
+    return !(env && env[0] == '0');
+}
+
+// The streaming path's persistent cross-item kernel applies (else one item per warp).
+bool dense_xi_applies(int N, int K, int split) {
+    return N % 32 == 0 && min_slice_steps(K, split) >= 4 && dense_cross_item();
+}
+
 template <int NT>
 int launch_dense_nt(const DenseParams &p, cudaStream_t st) {
     const long items = (long)((p.N + 31) / 32) * p.split * p.ntg;
-    const long blocks = (items * 32 + kDenseThreads - 1) / kDenseThreads;
     trace_before(kTraceDense, st);
-    dense_stream_kernel<NT, 4><<<(unsigned)blocks, kDenseThreads, 0, st>>>(p);
+    if (dense_xi_applies(p.N, p.K, p.split)) {
+        // as many warps as keep every warp at the same item count within the resident set
+        static int resident[2] = {0, 0};
+        int &res = resident[NT - 1];
+        if (!res) {
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dense_stream_xi_kernel<NT>,
+                                                              kDenseThreads, 0) != cudaSuccess ||
+                per_sm < 1)
+                per_sm = 1;
+            res = per_sm * sm_count() * (kDenseThreads / 32);
+        }
+        const long per_warp = (items + res - 1) / res;
+        const long nwarps = (items + per_warp - 1) / per_warp;
+        const long blocks = (nwarps * 32 + kDenseThreads - 1) / kDenseThreads;
+        dense_stream_xi_kernel<NT><<<(unsigned)blocks, kDenseThreads, 0, st>>>(p, (int)nwarps);
+    } else {
+        const long blocks = (items * 32 + kDenseThreads - 1) / kDenseThreads;
+        dense_stream_kernel<NT, 4><<<(unsigned)blocks, kDenseThreads, 0, st>>>(p);
+    }
     trace_after(kTraceDense, st);
     return launch_status();
 }
@@ -434,7 +526,7 @@ int dense_tokens_per_tile(int M) {
 }
 
 // Split so that (32-row blocks x token groups x split) gives about 24 warp items per SM,
-// with at least 4 K steps (128 K values) per item.
+// with at least 4 K steps (128 K values) per item and no empty slice.
 int dense_auto_split(int M, int N, int K) {
     const char *env = getenv("HLA_DENSE_SPLIT");
     const long nrb = (N + 31) / 32;
@@ -446,7 +538,10 @@ int dense_auto_split(int M, int N, int K) {
     if (s < 1) s = 1;
     if (s > maxs) s = maxs;
     if (s > 64) s = 64;
-    return (int)s;
+    // fewest slices of the same length: no slice left empty (128 K steps in 17 slices of 8
+    // would leave the last one with nothing to stream)
+    const long steps = K / 32, per = (steps + s - 1) / s;
+    return (int)((steps + per - 1) / per);
 }
 
 int router_split(int M, int Hd, int E) { return dense_auto_split(M, E, Hd); }
@@ -537,7 +632,8 @@ extern "C" int skinny_proj_splitk(int M, int N, int K, const hla_bf16 *x, const 
     HLA_REQUIRE(need == 0 || (ws && ws_bytes >= need), HLA_ERR_WORKSPACE);
     HLA_REQUIRE(need == 0 || aligned16(ws), HLA_ERR_MISALIGNED);
     cudaStream_t st = (cudaStream_t)stream;
-    set_variant("skinny_proj<tt%d,split%d>", dense_tokens_per_tile(M), s);
+    set_variant("skinny_proj<tt%d,%ssplit%d>", dense_tokens_per_tile(M),
+                !dense_tc_enabled(M) && dense_xi_applies(N, K, s) ? "xi," : "", s);
     if (s == 1) return run_dense(M, N, K, x, W, 1, nullptr, y, y_dtype == HLA_BF16, residual, st);
     int r = run_dense(M, N, K, x, W, s, reinterpret_cast<float *>(ws), nullptr, 0, nullptr, st);
     if (r != HLA_OK) return r;
@@ -611,7 +707,7 @@ extern "C" int hla_l2_prefetch(const void *ptr, size_t bytes, hla_stream stream)
 // Default split of the projection fused with residual + RMSNorm: that epilogue sums every
 // slice of a row in one CTA, so on the streaming path the split is capped at 8 (at batch 1
 // and 8 with N = 7168, K = 4096: 17.6 / 17.9 us at split 8 against 19.9 / 20.5 us at the
-// generic choice of 17).
+// generic choice, then 17).
 static int residual_norm_split(int M, int N, int K, int split) {
     const int s = resolve_split(M, N, K, split);
     return (split == 0 && !dense_tc_enabled(M) && s > 8) ? 8 : s;

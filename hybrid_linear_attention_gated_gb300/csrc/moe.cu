@@ -91,19 +91,6 @@ bool moe_cross_item() {
     return !(env && env[0] == '0');
 }
 
-// Fewest K steps of 32 in any of the `split` slices of [0, K) that k_slice hands out.
-int min_slice_steps(int K, int split) {
-    const int steps = K >> 5;
-    const int per = (steps + split - 1) / split;
-    int mn = steps;
-    for (int s = 0; s < split; ++s) {
-        const int kb = s * per < steps ? s * per : steps;
-        const int ke = (s + 1) * per < steps ? (s + 1) * per : steps;
-        if (ke - kb < mn) mn = ke - kb;
-    }
-    return mn;
-}
-
 int moe_items_split(int M, int k, int E, int nsh, long row_blocks, long cap) {
     long units = (long)M * k < E ? (long)M * k : E;
     units += nsh;
@@ -452,102 +439,19 @@ __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(const MoeArgs a) 
     }
 }
 
-// ---------------------------------------------------------------------------------------
-// Cross-item pipeline.  In the two kernels above a warp's loads stop at the end of every
-// work item: its ring drains, the next item is claimed and decoded, and only then are that
-// item's first loads issued, so each item boundary leaves the warp with nothing in flight
-// for about one atomic plus one memory latency.  With items of 64-128 KB of weights (the
-// down projection, and both products at small batch) that gap is a visible share of an
-// item.  stream_items keeps the ring of UNROLL K steps running across item boundaries: the
-// next item is claimed kClaimAhead steps before its first loads are due (late, so that the
-// dynamic balance between warps stays as it was: at batch 1 a warp has about two items)
-// and decoded just before them, and the last steps of one item are multiplied while the
-// first loads of the next are already in flight.  Every item must have at least UNROLL K
-// steps (the host checks the K slices), so the loads ahead reach at most into the next item.
-constexpr int kClaimAhead = 2;
-
-// lane 0 claims; the index is broadcast when it is used, a few steps later
-__device__ __forceinline__ int claim_lane0(int *counter) {
-    return (threadIdx.x & 31) == 0 ? atomicAdd(counter, 1) : 0;
-}
-
-// What a warp streams for one work item: weight row g of each matrix (row g + 8 lies ld8
-// elements further on) and the token row of each 8-token tile, all offset to the item's
-// first K value; n K steps of 32 (0: no item); ctx is what the item's epilogue needs.
-template <int NMAT, int NT, class Ctx>
-struct ItemRows {
-    const uint16_t *w[NMAT];
-    const uint16_t *x[NT];
-    int n;
-    Ctx ctx;
-    __device__ __forceinline__ void load(int s, size_t ld8, uint4 (&wa)[NMAT][2],
-                                         uint4 (&xb)[NT]) const {
-        const int k = 32 * s + (threadIdx.x & 3) * 8;
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-            wa[m][0] = ld_weight_v4(w[m] + k);
-            wa[m][1] = ld_weight_v4(w[m] + ld8 + k);
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) xb[nt] = ld_act_v4(x[nt] + k);
-    }
-};
-
-template <int NMAT, int NT>
-__device__ __forceinline__ void zero_acc(float (&acc)[NMAT][NT][4]) {
-#pragma unroll
-    for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[m][nt][q] = 0.f;
-}
-
-// decode(it) -> ItemRows of work item it (< total); epilogue(ctx, acc) stores an item's result.
-template <int NMAT, int NT, int UNROLL, class Ctx, class Decode, class Epilogue>
-__device__ __forceinline__ void stream_items(int *counter, int total, size_t ld8,
-                                             const Decode &decode, const Epilogue &epilogue) {
-    using Item = ItemRows<NMAT, NT, Ctx>;
-    int it = claim_item(counter);
-    if (it >= total) return;
-    Item cur = decode(it);
-    Item nxt;
-    nxt.n = 0;
+// Work-item claims for stream_items (stream_mma.cuh): lane 0 takes the next index from the
+// counter a few K steps before the item's first loads are due; the index is broadcast to the
+// warp when the item is decoded, so the atomic's latency passes meanwhile.  Claiming late
+// keeps the dynamic balance between warps as it was (at batch 1 a warp has about two items).
+struct CounterClaims {
+    int *counter;
     int pend = 0;
-    uint4 wa[UNROLL][NMAT][2];
-    uint4 xb[UNROLL][NT];
-    float acc[NMAT][NT][4];
-    zero_acc<NMAT, NT>(acc);
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) cur.load(u, ld8, wa[u], xb[u]);
-    int ls = 0;  // the step of cur that ring slot u holds
-    for (;;) {
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int first_next = cur.n - UNROLL;  // the step whose refill is next's step 0
-            if (ls == (first_next > kClaimAhead ? first_next - kClaimAhead : 0))
-                pend = claim_lane0(counter);
-            mma_step<NMAT, NT>(wa[u], xb[u], acc);
-            if (ls == first_next) {
-                it = __shfl_sync(0xffffffffu, pend, 0);
-                if (it < total) nxt = decode(it);
-            }
-            int j = ls + UNROLL;  // the step that refills slot u, counted from cur's first
-            if (ls == cur.n - 1) {
-                epilogue(cur.ctx, acc);
-                zero_acc<NMAT, NT>(acc);
-                if (nxt.n == 0) return;
-                cur = nxt;
-                nxt.n = 0;
-                ls = -1;
-                j = UNROLL - 1;
-            }
-            if (j < cur.n) cur.load(j, ld8, wa[u], xb[u]);
-            else if (j - cur.n < nxt.n) nxt.load(j - cur.n, ld8, wa[u], xb[u]);
-            ++ls;
-        }
+    __device__ __forceinline__ int first() { return claim_item(counter); }
+    __device__ __forceinline__ void issue() {
+        pend = (threadIdx.x & 31) == 0 ? atomicAdd(counter, 1) : 0;
     }
-}
+    __device__ __forceinline__ int take() { return __shfl_sync(0xffffffffu, pend, 0); }
+};
 
 struct GateupCtx {
     int pt, p1, ks, rb;  // first position of the token group, end of the unit, K slice, row block
@@ -610,7 +514,8 @@ __global__ void __launch_bounds__(kMoeThreads, xi_min_blocks(NT, UNROLL))
             }
         }
     };
-    stream_items<2, NT, UNROLL, GateupCtx>(&a.meta[3], total, (size_t)8 * a.Hd, decode, epilogue);
+    CounterClaims claims{&a.meta[3]};
+    stream_items<2, NT, UNROLL, GateupCtx>(claims, total, (size_t)8 * a.Hd, decode, epilogue);
 }
 
 template <int NT>
@@ -673,7 +578,8 @@ __global__ void __launch_bounds__(kMoeThreads, xi_min_blocks(NT, 4)) moe_down_xi
             }
         }
     };
-    stream_items<2, NT, 4, DownCtx<NT>>(&a.meta[4], total, (size_t)8 * a.I, decode, epilogue);
+    CounterClaims claims{&a.meta[4]};
+    stream_items<2, NT, 4, DownCtx<NT>>(claims, total, (size_t)8 * a.I, decode, epilogue);
 }
 
 // y[m] = sum_j w[m,j] * (sum over down slices of y[m,j]) (+ residual): slots in increasing

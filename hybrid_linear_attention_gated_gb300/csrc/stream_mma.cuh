@@ -101,4 +101,116 @@ __device__ __forceinline__ void k_slice(int K, int split, int ks, int &kb, int &
     ke = min(steps, (ks + 1) * per) * 32;
 }
 
+// Fewest K steps of 32 in any of the `split` slices of [0, K) that k_slice hands out.
+inline int min_slice_steps(int K, int split) {
+    const int steps = K >> 5;
+    const int per = (steps + split - 1) / split;
+    int mn = steps;
+    for (int s = 0; s < split; ++s) {
+        const int kb = s * per < steps ? s * per : steps;
+        const int ke = (s + 1) * per < steps ? (s + 1) * per : steps;
+        if (ke - kb < mn) mn = ke - kb;
+    }
+    return mn;
+}
+
+// ---------------------------------------------------------------------------------------
+// Cross-item pipeline.  A warp that runs warp_stream_tile once per work item stops loading
+// at the end of every item: its ring drains, the next item is found and decoded, and only
+// then are that item's first loads issued, so each item boundary leaves the warp with
+// nothing in flight for about one memory latency (plus, with dynamic claiming, one atomic).
+// With items of 64-128 KB of weights that gap is a visible share of an item.  stream_items
+// keeps a ring of UNROLL K steps running across item boundaries: the next item is claimed
+// kClaimAhead steps before its first loads are due, decoded just before them, and the last
+// steps of one item are multiplied while the first loads of the next are in flight.  Every
+// item must have at least UNROLL K steps (the caller checks the K slices with
+// min_slice_steps), so the loads ahead reach at most into the next item.
+constexpr int kClaimAhead = 2;
+
+// What a warp streams for one work item: weight row g of each matrix (row g + 8 lies ld8
+// elements further on) and the token row of each 8-token tile, all offset to the item's
+// first K value; n K steps of 32 (0: no item); ctx is what the item's epilogue needs.
+template <int NMAT, int NT, class Ctx>
+struct ItemRows {
+    const uint16_t *w[NMAT];
+    const uint16_t *x[NT];
+    int n;
+    Ctx ctx;
+    __device__ __forceinline__ void load(int s, size_t ld8, uint4 (&wa)[NMAT][2],
+                                         uint4 (&xb)[NT]) const {
+        const int k = 32 * s + (threadIdx.x & 3) * 8;
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+            wa[m][0] = ld_weight_v4(w[m] + k);
+            wa[m][1] = ld_weight_v4(w[m] + ld8 + k);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) xb[nt] = ld_act_v4(x[nt] + k);
+    }
+};
+
+template <int NMAT, int NT>
+__device__ __forceinline__ void zero_acc(float (&acc)[NMAT][NT][4]) {
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[m][nt][q] = 0.f;
+}
+
+// Items handed out round-robin: warp w of nw takes items w, w + nw, w + 2 nw, ...
+struct StridedClaims {
+    int it, stride;
+    __device__ __forceinline__ int first() { return it; }
+    __device__ __forceinline__ void issue() {}
+    __device__ __forceinline__ int take() { return it += stride; }
+};
+
+// claims: first() -> the warp's first item, issue() at the claim point, take() -> the next
+// item (>= total: none).  decode(it) -> ItemRows of item it; epilogue(ctx, acc) stores an
+// item's result.
+template <int NMAT, int NT, int UNROLL, class Ctx, class Claims, class Decode, class Epilogue>
+__device__ __forceinline__ void stream_items(Claims &claims, int total, size_t ld8,
+                                             const Decode &decode, const Epilogue &epilogue) {
+    using Item = ItemRows<NMAT, NT, Ctx>;
+    int it = claims.first();
+    if (it >= total) return;
+    Item cur = decode(it);
+    Item nxt;
+    nxt.n = 0;
+    uint4 wa[UNROLL][NMAT][2];
+    uint4 xb[UNROLL][NT];
+    float acc[NMAT][NT][4];
+    zero_acc<NMAT, NT>(acc);
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) cur.load(u, ld8, wa[u], xb[u]);
+    int ls = 0;  // the step of cur that ring slot u holds
+    for (;;) {
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int first_next = cur.n - UNROLL;  // the step whose refill is next's step 0
+            if (ls == (first_next > kClaimAhead ? first_next - kClaimAhead : 0)) claims.issue();
+            mma_step<NMAT, NT>(wa[u], xb[u], acc);
+            if (ls == first_next) {
+                it = claims.take();
+                if (it < total) nxt = decode(it);
+            }
+            int j = ls + UNROLL;  // the step that refills slot u, counted from cur's first
+            if (ls == cur.n - 1) {
+                epilogue(cur.ctx, acc);
+                zero_acc<NMAT, NT>(acc);
+                if (nxt.n == 0) return;
+                cur = nxt;
+                nxt.n = 0;
+                ls = -1;
+                j = UNROLL - 1;
+            }
+            if (j < cur.n) cur.load(j, ld8, wa[u], xb[u]);
+            else if (j - cur.n < nxt.n) nxt.load(j - cur.n, ld8, wa[u], xb[u]);
+            ++ls;
+        }
+    }
+}
+
 }  // namespace hla

@@ -189,6 +189,10 @@ int spec_accept_prefix(int B, int T, const int32_t *draft_ids, const int32_t *ta
  *  split = number of K slices (0 = automatic by M, N, K).  split > 1 writes
  *  fp32 partials into the workspace and a second kernel sums them in increasing
  *  slice order, then adds the residual (fixed order: deterministic).
+ *  Below 32 tokens, with N % 32 == 0 and every K slice at least 128 values long,
+ *  persistent warps keep their weight loads running from one work item into the
+ *  next (variant "xi"; HLA_DENSE_XITEM=0 runs one item per warp instead, with the
+ *  same results bit for bit).
  * -------------------------------------------------------------------------*/
 size_t skinny_proj_splitk_workspace_size(int M, int N, int K, int split);
 int skinny_proj_splitk(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W,
@@ -261,6 +265,10 @@ int moe_route_topk(int M, int Hd, int E, int k, const hla_bf16 *x, const hla_bf1
  *  NULL; y bf16 [M, Hd].  Hd % 32 == 0, I % 32 == 0, 1 <= M <= 256,
  *  1 <= k <= 16, E + n_shared <= 1024, 0 <= n_shared <= 16.
  *  Each active expert's weights are read once per call for all of its tokens.
+ *  Persistent warps claim work items and keep their weight loads running from one
+ *  item into the next when every K slice is long enough (variant flags "xgu" and
+ *  "xdn"; HLA_MOE_XITEM=0 stops the loads at each item instead, with the same
+ *  results bit for bit).
  *  prefetch_stream: NULL, or a second stream on which an L2 prefetch of the
  *  shared experts' weights runs while routing bookkeeping runs on `stream`;
  *  `stream` joins it before returning, so the call stays capturable as one

@@ -63,6 +63,35 @@ def test_skinny_proj(dev, M, N, K, split, res, out):
     assert frob_rel(f64(y), ref) < tol
 
 
+@pytest.mark.parametrize("M,N,K,split,res,out", [
+    (1, 1024, 544, 1, False, hla.HLA_F32), (1, 16416, 7168, 0, False, hla.HLA_F32),
+    (5, 256, 7168, 7, True, hla.HLA_BF16), (8, 2048, 1024, 3, True, hla.HLA_F32),
+    (12, 512, 2048, 5, False, hla.HLA_BF16), (31, 7168, 4096, 0, True, hla.HLA_BF16)])
+def test_dense_cross_item_bitwise(dev, M, N, K, split, res, out, monkeypatch):
+    """The persistent streaming kernel whose load ring runs across items gives the same bits as
+    one item per warp, and matches the oracle.  K slices of 17, 11/10 and 13/12 steps move the
+    ring's phase at item boundaries; 8- and 16-token tiles, split and direct epilogues."""
+    g = inputs.generator(700 + M + N)
+    x = inputs.activations(M, K, g).to(dev)
+    W = inputs.weight((N, K), g).to(dev)
+    r = inputs.activations(M, N, g).to(dev) if res else None
+    dt = torch.bfloat16 if out == hla.HLA_BF16 else torch.float32
+    nb = hla.skinny_proj_splitk_workspace_size(M, N, K, split)
+    ws = _ws(nb, dev)
+    ys, variants = {}, {}
+    for xi in ("1", "0"):
+        monkeypatch.setenv("HLA_DENSE_XITEM", xi)
+        ys[xi] = torch.empty(M, N, device=dev, dtype=dt)
+        hla.skinny_proj_splitk(M, N, K, x, W, r, ys[xi], out, split, ws, ws.numel())
+        variants[xi] = hla.hla_last_variant()
+    torch.cuda.synchronize()
+    assert ",xi," in variants["1"] and ",xi," not in variants["0"], variants
+    assert torch.equal(ys["1"], ys["0"])
+    ref = oracle.moe.linear(f64(x), f64(W)) + (f64(r) if res else 0.0)
+    tol = PROJ_FROB_REL_BF16 if out == hla.HLA_BF16 else PROJ_FROB_REL_F32
+    assert frob_rel(f64(ys["1"]), ref) < tol
+
+
 @pytest.mark.parametrize("M", [1, 8, 64])
 def test_proj_residual_rmsnorm(dev, M):
     """o-projection + residual + RMSNorm in one epilogue: bit-identical to skinny_proj_splitk
