@@ -728,7 +728,7 @@ def run_profile(kind, iters=3):
     info = dict(case=kind)
     if kind == "moe":
         # 48 experts, 32 tokens, top-8: the same kernel variants as the batch-64 workload
-        # (16-token tile, the 2-step gate/up pipeline used from 32 tokens), 4.2 GB of weights
+        # (16-token tile, cross-item load rings, no K split), 4.2 GB of weights
         E, M = 48, 32
         w = inputs.moe_weights(E, c["Hd"], c["I"], c["n_shared"], g, device=dev)
         x = inputs.activations(M, c["Hd"], g, dev)

@@ -27,6 +27,7 @@
 // opt-in placements compute them instead as dense SwiGLU products into their output slots:
 // on the tensor-core path before dispatch (HLA_SHARED_TC=1, past 16 tokens), or on the side
 // stream concurrently with everything routed (HLA_SHARED_STREAM=1, moe_shared_side).
+#include <cstdio>
 #include <cstdlib>
 
 #include "common.cuh"
@@ -79,7 +80,8 @@ int moe_tokens_per_tile(int M) { return M <= 8 ? 8 : 16; }
 //    claimed end soon after the others (at batch 8: 726 us with splits 4 / 2 against 775 us
 //    unsplit; at batch 32 and 64 splitting measured no better or slower, the partials then
 //    being large).
-// HLA_MOE_SHALLOW=0 keeps the 4-step gate/up pipeline at every batch (A/B measurements).
+// HLA_MOE_SHALLOW=0 keeps the per-item gate/up kernel at 4 K steps of loads from 32 tokens too
+// (A/B measurements); the cross-item kernels take their ring depth from moe_ring_depth.
 bool moe_shallow_gateup() {
     const char *env = getenv("HLA_MOE_SHALLOW");
     return !(env && env[0] == '0');
@@ -454,7 +456,8 @@ struct CounterClaims {
 };
 
 struct GateupCtx {
-    int pt, p1, ks, rb;  // first position of the token group, end of the unit, K slice, row block
+    int ptn;   // first position of the token group << 5 | its number of tokens (1..16)
+    int rbks;  // row block << 8 | K slice
 };
 
 // Resident CTAs per SM the cross-item kernels keep (at most 65536 / (128 x 128) registers
@@ -492,22 +495,24 @@ __global__ void __launch_bounds__(kMoeThreads, xi_min_blocks(NT, UNROLL))
             r.x[nt] = a.x + (size_t)a.pos_token[p < p1 ? p : pt] * a.Hd + kb;
         }
         r.n = (ke - kb) >> 5;
-        r.ctx = GateupCtx{pt, p1, ks, rb};
+        r.ctx = GateupCtx{pt << 5 | min(p1 - pt, a.TT), rb << 8 | ks};
         return r;
     };
     auto epilogue = [&](const GateupCtx &c, float (&acc)[2][NT][4]) {
+        const int pt = c.ptn >> 5, n = c.ptn & 31, rb = c.rbks >> 8, ks = c.rbks & 255;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int row = c.rb * 16 + acc_row(q);
-                const int p = c.pt + acc_tok(nt, q);
-                if (p >= c.p1) continue;
+                const int row = rb * 16 + acc_row(q);
+                const int t = acc_tok(nt, q);
+                if (t >= n) continue;
+                const int p = pt + t;
                 if (a.KS == 1) {
                     a.h[(size_t)p * a.I + row] =
                         float_to_bf16_bits(__fmul_rn(silu_f(acc[0][nt][q]), acc[1][nt][q]));
                 } else {
-                    const size_t o = ((size_t)c.ks * a.P + p) * a.I + row;
+                    const size_t o = ((size_t)ks * a.P + p) * a.I + row;
                     a.part_g[o] = acc[0][nt][q];
                     a.part_u[o] = acc[1][nt][q];
                 }
@@ -524,8 +529,9 @@ struct DownCtx {
     int slot[NT][2];   // output slot of the two tokens this lane holds in tile nt (-1: none)
 };
 
-template <int NT>
-__global__ void __launch_bounds__(kMoeThreads, xi_min_blocks(NT, 4)) moe_down_xi_kernel(const MoeArgs a) {
+template <int NT, int UNROLL>
+__global__ void __launch_bounds__(kMoeThreads, xi_min_blocks(NT, UNROLL))
+    moe_down_xi_kernel(const MoeArgs a) {
     const int U = a.meta[0];
     const int total = a.item_dn[U];
     const int g = (threadIdx.x & 31) >> 2;
@@ -579,7 +585,7 @@ __global__ void __launch_bounds__(kMoeThreads, xi_min_blocks(NT, 4)) moe_down_xi
         }
     };
     CounterClaims claims{&a.meta[4]};
-    stream_items<2, NT, 4, DownCtx<NT>>(claims, total, (size_t)8 * a.I, decode, epilogue);
+    stream_items<2, NT, UNROLL, DownCtx<NT>>(claims, total, (size_t)8 * a.I, decode, epilogue);
 }
 
 // y[m] = sum_j w[m,j] * (sum over down slices of y[m,j]) (+ residual): slots in increasing
@@ -688,6 +694,61 @@ int persistent_grid(K kernel) {
         per_sm < 1)
         per_sm = 1;
     return per_sm * sm_count();
+}
+
+// K steps in the load ring of the cross-item expert kernels: 4 for both at every batch
+// (HLA_MOE_RING_GU / HLA_MOE_RING_DN = 2..4 override it for A/B runs).  Measured on the layer
+// (CUDA graphs, same box, results bit-identical across depths): gate/up with 4 steps against 2
+// took 2957 / 3041 us at batch 64 and 2132 / 2196 us at batch 32 (the 2-step ring that the
+// per-item kernel prefers from 32 tokens), 819 / 828 us at batch 8 (3 steps: 845 us); down with
+// 2 or 3 steps was slower at every batch (3222 / 3198 us against 3041 us at batch 64).
+int moe_ring_depth(bool gateup) {
+    const char *env = getenv(gateup ? "HLA_MOE_RING_GU" : "HLA_MOE_RING_DN");
+    if (env) {
+        const int v = atoi(env);
+        if (v >= 2 && v <= 4) return v;
+    }
+    return 4;
+}
+
+template <int NT, int R, typename F>
+void launch_gateup_ring(F budgeted, const MoeArgs &a, cudaStream_t st) {
+    static int g = 0;
+    if (!g) g = persistent_grid(moe_gateup_xi_kernel<NT, R>);
+    moe_gateup_xi_kernel<NT, R><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+}
+
+template <int NT, int R, typename F>
+void launch_down_ring(F budgeted, const MoeArgs &a, cudaStream_t st) {
+    static int g = 0;
+    if (!g) g = persistent_grid(moe_down_xi_kernel<NT, R>);
+    moe_down_xi_kernel<NT, R><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+}
+
+template <typename F>
+void launch_gateup_xi(int TT, int ring, F budgeted, const MoeArgs &a, cudaStream_t st) {
+    if (TT == 8) {
+        if (ring == 2) launch_gateup_ring<1, 2>(budgeted, a, st);
+        else if (ring == 3) launch_gateup_ring<1, 3>(budgeted, a, st);
+        else launch_gateup_ring<1, 4>(budgeted, a, st);
+    } else {
+        if (ring == 2) launch_gateup_ring<2, 2>(budgeted, a, st);
+        else if (ring == 3) launch_gateup_ring<2, 3>(budgeted, a, st);
+        else launch_gateup_ring<2, 4>(budgeted, a, st);
+    }
+}
+
+template <typename F>
+void launch_down_xi(int TT, int ring, F budgeted, const MoeArgs &a, cudaStream_t st) {
+    if (TT == 8) {
+        if (ring == 2) launch_down_ring<1, 2>(budgeted, a, st);
+        else if (ring == 3) launch_down_ring<1, 3>(budgeted, a, st);
+        else launch_down_ring<1, 4>(budgeted, a, st);
+    } else {
+        if (ring == 2) launch_down_ring<2, 2>(budgeted, a, st);
+        else if (ring == 3) launch_down_ring<2, 3>(budgeted, a, st);
+        else launch_down_ring<2, 4>(budgeted, a, st);
+    }
 }
 
 struct SideStreamEvents {
@@ -834,6 +895,15 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
         if ((r = moe_shared_side(M, Hd, I, E, k, nsh, x, Ws_gate, Ws_up, Ws_down, ws, st, pf)) != HLA_OK)
             return r;
     }
+    // Per-item gate/up kernel (K slices shorter than the ring): loads 4 K steps ahead, or 2
+    // from 32 tokens (fewer registers, 4 resident CTAs per SM instead of 3; measured on the
+    // decode layer, CUDA graph, same box: gate/up at batch 64 1910 us against 1958, batch 32
+    // 2224 us against 2283, slower at batch 16).
+    const bool shallow = L.TT == 16 && M >= 32 && moe_shallow_gateup();
+    // The cross-item kernels need every K slice to hold at least the ring's depth in steps.
+    const int ring_gu = moe_ring_depth(true), ring_dn = moe_ring_depth(false);
+    const bool xgu = moe_cross_item() && min_slice_steps(Hd, L.KS) >= ring_gu;
+    const bool xdn = moe_cross_item() && min_slice_steps(I, L.KSD) >= ring_dn;
     const int dthreads = (int)round_up((size_t)(E + nsh), 32);
     moe_dispatch_kernel<<<1, dthreads, 0, st>>>(a);
     r = launch_status();
@@ -841,45 +911,20 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     const int keep = shared_side ? sm_count() - shared_sm_budget() : sm_count();
     auto budgeted = [&](int full) { return full / sm_count() * keep; };
     trace_before(kTraceMoeGateup, st);
-    // K steps of loads in flight per warp in the gate/up kernel: 4, or 2 from 32 tokens (fewer
-    // registers, 4 resident CTAs per SM instead of 3).  Measured on the decode layer (CUDA
-    // graph, same box): with 2, gate/up at batch 64 took 1910 us against 1958 and the layer
-    // 3075 us against 3100, batch 32 2224 us against 2283; at batch 16 it was slower (1940 us
-    // against 1609), and the down kernel did not gain.
-    const bool shallow = L.TT == 16 && M >= 32 && moe_shallow_gateup();
-    // The cross-item kernels need every K slice to hold at least the ring's depth in steps.
-    const bool xgu = moe_cross_item() && min_slice_steps(Hd, L.KS) >= (shallow ? 2 : 4);
-    const bool xdn = moe_cross_item() && min_slice_steps(I, L.KSD) >= 4;
-    if (L.TT == 8) {
-        if (xgu) {
-            static int g = 0;
-            if (!g) g = persistent_grid(moe_gateup_xi_kernel<1, 4>);
-            moe_gateup_xi_kernel<1, 4><<<budgeted(g), kMoeThreads, 0, st>>>(a);
-        } else {
-            static int g = 0;
-            if (!g) g = persistent_grid(moe_gateup_kernel<1, 4>);
-            moe_gateup_kernel<1, 4><<<budgeted(g), kMoeThreads, 0, st>>>(a);
-        }
+    if (xgu) {
+        launch_gateup_xi(L.TT, ring_gu, budgeted, a, st);
+    } else if (L.TT == 8) {
+        static int g = 0;
+        if (!g) g = persistent_grid(moe_gateup_kernel<1, 4>);
+        moe_gateup_kernel<1, 4><<<budgeted(g), kMoeThreads, 0, st>>>(a);
     } else if (shallow) {
-        if (xgu) {
-            static int g = 0;
-            if (!g) g = persistent_grid(moe_gateup_xi_kernel<2, 2>);
-            moe_gateup_xi_kernel<2, 2><<<budgeted(g), kMoeThreads, 0, st>>>(a);
-        } else {
-            static int g = 0;
-            if (!g) g = persistent_grid(moe_gateup_kernel<2, 2>);
-            moe_gateup_kernel<2, 2><<<budgeted(g), kMoeThreads, 0, st>>>(a);
-        }
+        static int g = 0;
+        if (!g) g = persistent_grid(moe_gateup_kernel<2, 2>);
+        moe_gateup_kernel<2, 2><<<budgeted(g), kMoeThreads, 0, st>>>(a);
     } else {
-        if (xgu) {
-            static int g = 0;
-            if (!g) g = persistent_grid(moe_gateup_xi_kernel<2, 4>);
-            moe_gateup_xi_kernel<2, 4><<<budgeted(g), kMoeThreads, 0, st>>>(a);
-        } else {
-            static int g = 0;
-            if (!g) g = persistent_grid(moe_gateup_kernel<2, 4>);
-            moe_gateup_kernel<2, 4><<<budgeted(g), kMoeThreads, 0, st>>>(a);
-        }
+        static int g = 0;
+        if (!g) g = persistent_grid(moe_gateup_kernel<2, 4>);
+        moe_gateup_kernel<2, 4><<<budgeted(g), kMoeThreads, 0, st>>>(a);
     }
     trace_after(kTraceMoeGateup, st);
     if ((r = launch_status()) != HLA_OK) return r;
@@ -888,26 +933,16 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
         if ((r = launch_status()) != HLA_OK) return r;
     }
     trace_before(kTraceMoeDown, st);
-    if (L.TT == 8) {
-        if (xdn) {
-            static int d = 0;
-            if (!d) d = persistent_grid(moe_down_xi_kernel<1>);
-            moe_down_xi_kernel<1><<<budgeted(d), kMoeThreads, 0, st>>>(a);
-        } else {
-            static int d = 0;
-            if (!d) d = persistent_grid(moe_down_kernel<1>);
-            moe_down_kernel<1><<<budgeted(d), kMoeThreads, 0, st>>>(a);
-        }
+    if (xdn) {
+        launch_down_xi(L.TT, ring_dn, budgeted, a, st);
+    } else if (L.TT == 8) {
+        static int d = 0;
+        if (!d) d = persistent_grid(moe_down_kernel<1>);
+        moe_down_kernel<1><<<budgeted(d), kMoeThreads, 0, st>>>(a);
     } else {
-        if (xdn) {
-            static int d = 0;
-            if (!d) d = persistent_grid(moe_down_xi_kernel<2>);
-            moe_down_xi_kernel<2><<<budgeted(d), kMoeThreads, 0, st>>>(a);
-        } else {
-            static int d = 0;
-            if (!d) d = persistent_grid(moe_down_kernel<2>);
-            moe_down_kernel<2><<<budgeted(d), kMoeThreads, 0, st>>>(a);
-        }
+        static int d = 0;
+        if (!d) d = persistent_grid(moe_down_kernel<2>);
+        moe_down_kernel<2><<<budgeted(d), kMoeThreads, 0, st>>>(a);
     }
     trace_after(kTraceMoeDown, st);
     if ((r = launch_status()) != HLA_OK) return r;
@@ -916,8 +951,13 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     moe_combine_kernel<<<cgrid, 128, 0, st>>>(a);
     if ((r = launch_status()) != HLA_OK) return r;
     if (side && cudaStreamWaitEvent(st, g_moe_events.join, 0) != cudaSuccess) return HLA_ERR_CUDA;
-    set_variant("moe<tt%d,ks%d,ksd%d%s%s%s%s%s>", L.TT, L.KS, L.KSD, shallow ? ",u2" : "",
-                xgu ? ",xgu" : "", xdn ? ",xdn" : "",
+    // kernel forms: ",xgu<ring>" / ",xdn<ring>" cross-item, ",u2" the shallow per-item gate/up
+    char ringv[32] = "";
+    int o = 0;
+    if (xgu) o += snprintf(ringv, sizeof(ringv), ",xgu%d", ring_gu);
+    else if (shallow) o += snprintf(ringv, sizeof(ringv), ",u2");
+    if (xdn) snprintf(ringv + o, sizeof(ringv) - o, ",xdn%d", ring_dn);
+    set_variant("moe<tt%d,ks%d,ksd%d%s%s%s>", L.TT, L.KS, L.KSD, ringv,
                 L.shared_tc ? ",shared_tc" : (shared_side ? ",shared_side" : ""),
                 side ? ",prefetch" : "");
     return HLA_OK;
