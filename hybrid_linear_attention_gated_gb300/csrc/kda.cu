@@ -14,10 +14,13 @@
 //
 // Layout inside a CTA: 8 row groups x (CW/4) float4 column groups.  Thread
 // (rg, cg) keeps rows rg, rg+8, rg+16, ... of 4 columns in registers, so the state
-// is read from HBM once and written once.  The row partition (and therefore the
-// order of every reduction) is the same for every slice width, which makes the
-// result independent of the variant chosen: replaying T tokens is bit-identical to
-// T single decode steps.
+// is read from HBM once and written once.  The 8 row groups of a column group are
+// lanes of one warp (lane = 4 rg + cg % 4; warp w holds column groups 4w..4w+3), so
+// the sums over rows (u, w, q.k) finish with three butterfly shuffles inside the warp
+// and a step needs no block barrier.  The row partition (and therefore the order of
+// every reduction) is the same for every slice width, which makes the result
+// independent of the variant chosen: replaying T tokens is bit-identical to T single
+// decode steps.
 #include <cstdlib>
 
 #include "common.cuh"
@@ -64,14 +67,14 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
     constexpr bool COMMIT_END = MODE == kDecode || MODE == kReplay || MODE == kExtend;
     static_assert(TMAX <= NTHR, "one thread per token loads beta");
 
+    static_assert(CG % 4 == 0, "a warp holds 8 row groups x 4 column groups");
     __shared__ __align__(16) float sq[TMAX][DK], sk[TMAX][DK], sa[TMAX][DK], sv[TMAX][CW];
     __shared__ float sb[TMAX];
-    __shared__ float4 red_u[2][kRowGroups][CG], red_w[2][kRowGroups][CG];
-    __shared__ float red_qk[2][kRowGroups];
 
     const int tid = threadIdx.x;
-    const int cg = tid % CG;
-    const int rg = tid / CG;
+    const int lane = tid & 31;
+    const int rg = lane >> 2;
+    const int cg = (tid >> 5) * 4 + (lane & 3);
     const int slice = blockIdx.x % NSLICE;
     const int bh = blockIdx.x / NSLICE;
     const int h = bh % p.H;
@@ -195,7 +198,6 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
 
         for (int tt = 0; tt < tn; ++tt) {
             const int t = t0 + tt;
-            const int buf = t & 1;
             float4 pu = make_float4(0.f, 0.f, 0.f, 0.f), pw = pu;
             float pqk = 0.f;
 #pragma unroll
@@ -216,22 +218,22 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
                 pw.w = __fmaf_rn(qq, s[j].w, pw.w);
                 pqk = __fmaf_rn(qq, kk, pqk);
             }
-            red_u[buf][rg][cg] = pu;
-            red_w[buf][rg][cg] = pw;
-            if (cg == 0) red_qk[buf][rg] = pqk;
-            __syncthreads();
-
-            float4 u = red_u[buf][0][cg], w = red_w[buf][0][cg];
-            float qk = red_qk[buf][0];
+            // sums over the 8 row groups (lane bits 2..4): a butterfly, after which every lane
+            // holds the same bits (each level adds the same two values in either order)
 #pragma unroll
-            for (int r = 1; r < kRowGroups; ++r) {
-                const float4 ur = red_u[buf][r][cg], wr = red_w[buf][r][cg];
-                u.x = __fadd_rn(u.x, ur.x); u.y = __fadd_rn(u.y, ur.y);
-                u.z = __fadd_rn(u.z, ur.z); u.w = __fadd_rn(u.w, ur.w);
-                w.x = __fadd_rn(w.x, wr.x); w.y = __fadd_rn(w.y, wr.y);
-                w.z = __fadd_rn(w.z, wr.z); w.w = __fadd_rn(w.w, wr.w);
-                qk = __fadd_rn(qk, red_qk[buf][r]);
+            for (int m = 4; m < 32; m <<= 1) {
+                pu.x = __fadd_rn(pu.x, __shfl_xor_sync(0xffffffffu, pu.x, m));
+                pu.y = __fadd_rn(pu.y, __shfl_xor_sync(0xffffffffu, pu.y, m));
+                pu.z = __fadd_rn(pu.z, __shfl_xor_sync(0xffffffffu, pu.z, m));
+                pu.w = __fadd_rn(pu.w, __shfl_xor_sync(0xffffffffu, pu.w, m));
+                pw.x = __fadd_rn(pw.x, __shfl_xor_sync(0xffffffffu, pw.x, m));
+                pw.y = __fadd_rn(pw.y, __shfl_xor_sync(0xffffffffu, pw.y, m));
+                pw.z = __fadd_rn(pw.z, __shfl_xor_sync(0xffffffffu, pw.z, m));
+                pw.w = __fadd_rn(pw.w, __shfl_xor_sync(0xffffffffu, pw.w, m));
+                pqk = __fadd_rn(pqk, __shfl_xor_sync(0xffffffffu, pqk, m));
             }
+            const float4 u = pu, w = pw;
+            const float qk = pqk;
             const float bt = sb[tt];
             float4 d;
             d.x = __fmul_rn(bt, __fsub_rn(sv[tt][cg * 4 + 0], u.x));
