@@ -301,22 +301,24 @@ int launch_dk(int cw, const KdaParams &p, cudaStream_t st) {
 }
 
 // Column-slice width.  Measured on GB300 (d = 128, 32 heads, CUDA graphs, states rotated
-// over 512 MB):
-//   decode: 16 columns at batch 1-8 (batch 4: 4.79 us vs 5.34 with 32; batch 8: 6.85 vs 7.80
-//           with 64), 32 columns from batch 16 (batch 64: 40.9 us vs 42.5 with 64, 42.9 with 16);
-//   verify / replay / fused window (several tokens per CTA): 64 columns (batch 16 verify:
-//           15.4 us vs 18.2 with 32; batch 64: 46.5 vs 57.3).
-int choose_cw(int B, int H, int dv, bool decode) {
+// over 512 MB, the warp-shuffle row sums):
+//   decode: 16 columns, one warp per CTA, at every batch (batch 1: 2.85-3.2 us vs 3.56 with
+//           32; batch 32: 22.7 vs 23.4 with 32; batch 64: 42.1 vs 42.4);
+//   verify / replay / fused window (several tokens per CTA): 64 columns, halved while the
+//           heads do not cover the SMs twice (batch 16 separate window: 23.1 us vs 26.7 with
+//           32 and 32.2 with 16; batch 64: 81.5 vs 96.3 and 132);
+//   extend: whole heads (128 columns) while the heads fit one per SM, so each serial chain
+//           has an SM to itself (4 x 512-token chunks: 391 us vs 484 with 64 and 580 with 32),
+//           else 64 (60 decodes + 4 x 128-token chunks: 184 us vs 201 with 128).
+int choose_cw(int B, int H, int dv, int mode) {
     const char *env = getenv("HLA_KDA_CW");
     if (env) {
         const int v = atoi(env);
         if ((v == 16 || v == 32 || v == 64 || v == 128) && v <= dv) return v;
     }
     const long heads = (long)B * H;
-    if (decode) {
-        const int cw = heads <= 256 ? 16 : 32;
-        return cw <= dv ? cw : dv;
-    }
+    if (mode == kDecode) return 16 <= dv ? 16 : dv;
+    if (mode == kExtend) return heads <= sm_count() ? dv : (dv < 64 ? dv : 64);
     // 64-column slices (128 threads, 32 KB of state per CTA) once there are enough heads;
     // narrower slices put work on every SM at small batch.
     const long target = 2L * sm_count();
@@ -364,7 +366,7 @@ int run_kda(int mode, int B, int T, int H, int dk, int dv, float *S, const int32
     p.Tp = prev.T;
     p.accepted = accepted; p.o = o; p.o_bf16 = o_dtype == HLA_BF16; p.B = B; p.T = T; p.H = H;
     p.cu_seqlens = cu_seqlens;
-    int cw = choose_cw(B, H, dv, mode == kDecode);
+    int cw = choose_cw(B, H, dv, mode);
     if (mode == kReplayVerify && cw > 64) cw = 64;  // two windows of token vectors in shared memory
     static const char *names[5] = {"decode", "verify", "replay", "replay_verify", "extend"};
     set_variant("kda_recur<dk%d,cw%d,%s>", dk, cw, names[mode]);
