@@ -755,6 +755,25 @@ def run_profile(kind, iters=3):
         for _ in range(iters):
             hla.kda_decode_step(B, H, d, d, S, None, u["q"], u["k"], u["v"], u["alpha"], u["beta"], o)
         info.update(B=B, bytes=kda_bytes(B), variant=hla.hla_last_variant())
+    elif kind == "spec":
+        # speculative window at batch 64 (134 MB of committed state, > L2): verify, accept, replay
+        B, T, H, d = 64, c["spec_T"], c["H"], c["d"]
+        S = torch.randn(B, H, d, d, device=dev).mul_(0.05)
+        w = inputs.kda_inputs((B, T), H, d, d, g, dev)
+        dr, tg, a = inputs.accept_ids(B, T, g, dev)
+        o = torch.empty(B, T, H, d, device=dev)
+        acc = torch.zeros(B, dtype=torch.int32, device=dev)
+        com = torch.zeros(B, dtype=torch.int32, device=dev)
+        for _ in range(iters):
+            hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, S, None, w["q"], w["k"],
+                                       w["v"], w["alpha"], w["beta"], None, o)
+            verify_variant = hla.hla_last_variant()
+            hla.spec_accept_prefix(B, T, dr, tg, acc, com)
+            hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, S, None, w["q"], w["k"],
+                                       w["v"], w["alpha"], w["beta"], acc, None)
+        info.update(B=B, T=T, accepted=a.tolist(), verify_bytes=spec_bytes(B, T, a.cpu().numpy())["verify"],
+                    replay_bytes=spec_bytes(B, T, a.cpu().numpy())["replay"],
+                    variant=[verify_variant, hla.hla_last_variant()])
     elif kind in ("dense", "dense16"):
         # the input projection at batch 64 (tensor-core path) or 16 (streaming path)
         M, H, d = (64 if kind == "dense" else 16), c["H"], c["d"]
@@ -898,7 +917,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true")
-    ap.add_argument("--profile", choices=["moe", "kda", "dense", "dense16"],
+    ap.add_argument("--profile", choices=["moe", "kda", "spec", "dense", "dense16"],
                     help="run one small case of a hot kernel (for ncu captures) and exit")
     ap.add_argument("--prefetch-ab", action="store_true",
                     help="time the layer under every side-stream prefetch mask and exit")

@@ -544,7 +544,15 @@ int dense_auto_split(int M, int N, int K) {
     return (int)((steps + per - 1) / per);
 }
 
-int router_split(int M, int Hd, int E) { return dense_auto_split(M, E, Hd); }
+// HLA_ROUTER_SPLIT overrides the router's K split (A/B runs); the default is the projection rule.
+int router_split(int M, int Hd, int E) {
+    const char *env = getenv("HLA_ROUTER_SPLIT");
+    if (env) {
+        const int v = atoi(env);
+        if (v >= 1 && v <= Hd / 128) return v;
+    }
+    return dense_auto_split(M, E, Hd);
+}
 
 // Run x W^T with the streaming tile.  part != nullptr -> fp32 partials [split][M][N].
 int run_dense(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W, int split, float *part,

@@ -31,6 +31,11 @@ namespace {
 constexpr int kRowGroups = 8;
 constexpr int kMaxWindow = 8;
 
+// component e (a compile-time constant after unrolling) of a float4
+__device__ __forceinline__ float f4_at(const float4 v, int e) {
+    return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
 enum KdaMode { kDecode = 0, kVerify = 1, kReplay = 2, kReplayVerify = 3, kExtend = 4 };
 
 struct KdaParams {
@@ -68,8 +73,14 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
     static_assert(TMAX <= NTHR, "one thread per token loads beta");
 
     static_assert(CG % 4 == 0, "a warp holds 8 row groups x 4 column groups");
-    __shared__ __align__(16) float sq[TMAX][DK], sk[TMAX][DK], sa[TMAX][DK], sv[TMAX][CW];
+    // q, k and alpha of a token are stored row-group-major: row i at (i % 8) * PAD + i / 8, so a
+    // thread's rows rg, rg+8, ... are contiguous (float4 reads) and the 8 row groups of a warp
+    // start in distinct banks (PAD = RPT + 4)
+    constexpr int PAD = RPT + 4;
+    __shared__ __align__(16) float sq[TMAX][8 * PAD], sk[TMAX][8 * PAD], sa[TMAX][8 * PAD],
+        sv[TMAX][CW];
     __shared__ float sb[TMAX];
+    auto rowpos = [](int i) { return (i & 7) * PAD + (i >> 3); };
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -164,12 +175,24 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
                     if (x >= n_items) break;
                     const int tt = x / PER_TOK, c = x - tt * PER_TOK;
                     const uint4 w = r[u];
-                    if (c < 2 * QC + AC && c >= 2 * QC) {
-                        *reinterpret_cast<uint4 *>(&sa[tt][4 * (c - 2 * QC)]) = w;  // fp32 bits
+                    if (c < 2 * QC + AC && c >= 2 * QC) {  // 4 alphas (fp32 bits), rows i0..i0+3
+                        const int i0 = 4 * (c - 2 * QC);
+                        sa[tt][rowpos(i0 + 0)] = __uint_as_float(w.x);
+                        sa[tt][rowpos(i0 + 1)] = __uint_as_float(w.y);
+                        sa[tt][rowpos(i0 + 2)] = __uint_as_float(w.z);
+                        sa[tt][rowpos(i0 + 3)] = __uint_as_float(w.w);
                         continue;
                     }
-                    float *dst = c < QC ? &sq[tt][8 * c]
-                               : c < 2 * QC ? &sk[tt][8 * (c - QC)] : &sv[tt][8 * (c - 2 * QC - AC)];
+                    if (c < 2 * QC) {  // 8 bf16 of q or k, rows i0..i0+7 (one per row group)
+                        float *dst = c < QC ? sq[tt] : sk[tt];
+                        const int j = c < QC ? c : c - QC;  // i0 = 8 j: rows 8j .. 8j+7
+                        dst[0 * PAD + j] = bf16_lo(w.x); dst[1 * PAD + j] = bf16_hi(w.x);
+                        dst[2 * PAD + j] = bf16_lo(w.y); dst[3 * PAD + j] = bf16_hi(w.y);
+                        dst[4 * PAD + j] = bf16_lo(w.z); dst[5 * PAD + j] = bf16_hi(w.z);
+                        dst[6 * PAD + j] = bf16_lo(w.w); dst[7 * PAD + j] = bf16_hi(w.w);
+                        continue;
+                    }
+                    float *dst = &sv[tt][8 * (c - 2 * QC - AC)];
                     reinterpret_cast<float4 *>(dst)[0] =
                         make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
                     reinterpret_cast<float4 *>(dst)[1] =
@@ -186,9 +209,9 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
                 const float *al = pre ? p.alphap : p.alpha;
                 const size_t tok = token_row(t);
                 for (int i = tid; i < DK; i += NTHR) {
-                    sq[tt][i] = bf16_bits_to_float(q[tok * DK + i]);
-                    sk[tt][i] = bf16_bits_to_float(k[tok * DK + i]);
-                    sa[tt][i] = al[tok * DK + i];
+                    sq[tt][rowpos(i)] = bf16_bits_to_float(q[tok * DK + i]);
+                    sk[tt][rowpos(i)] = bf16_bits_to_float(k[tok * DK + i]);
+                    sa[tt][rowpos(i)] = al[tok * DK + i];
                 }
                 for (int c = tid; c < CW; c += NTHR) sv[tt][c] = bf16_bits_to_float(v[tok * DV + col0 + c]);
             }
@@ -200,10 +223,13 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
             const int t = t0 + tt;
             float4 pu = make_float4(0.f, 0.f, 0.f, 0.f), pw = pu;
             float pqk = 0.f;
+            const float4 *a4 = reinterpret_cast<const float4 *>(&sa[tt][rg * PAD]);
+            const float4 *k4 = reinterpret_cast<const float4 *>(&sk[tt][rg * PAD]);
+            const float4 *q4 = reinterpret_cast<const float4 *>(&sq[tt][rg * PAD]);
 #pragma unroll
-            for (int j = 0; j < RPT; ++j) {
-                const int i = rg + kRowGroups * j;
-                const float a = sa[tt][i], kk = sk[tt][i], qq = sq[tt][i];
+            for (int j = 0; j < RPT; ++j) {  // row rg + 8 j
+                const float a = f4_at(a4[j >> 2], j & 3), kk = f4_at(k4[j >> 2], j & 3),
+                            qq = f4_at(q4[j >> 2], j & 3);
                 s[j].x = __fmul_rn(s[j].x, a);
                 s[j].y = __fmul_rn(s[j].y, a);
                 s[j].z = __fmul_rn(s[j].z, a);
@@ -235,14 +261,15 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
             const float4 u = pu, w = pw;
             const float qk = pqk;
             const float bt = sb[tt];
+            const float4 vv = *reinterpret_cast<const float4 *>(&sv[tt][cg * 4]);
             float4 d;
-            d.x = __fmul_rn(bt, __fsub_rn(sv[tt][cg * 4 + 0], u.x));
-            d.y = __fmul_rn(bt, __fsub_rn(sv[tt][cg * 4 + 1], u.y));
-            d.z = __fmul_rn(bt, __fsub_rn(sv[tt][cg * 4 + 2], u.z));
-            d.w = __fmul_rn(bt, __fsub_rn(sv[tt][cg * 4 + 3], u.w));
+            d.x = __fmul_rn(bt, __fsub_rn(vv.x, u.x));
+            d.y = __fmul_rn(bt, __fsub_rn(vv.y, u.y));
+            d.z = __fmul_rn(bt, __fsub_rn(vv.z, u.z));
+            d.w = __fmul_rn(bt, __fsub_rn(vv.w, u.w));
 #pragma unroll
             for (int j = 0; j < RPT; ++j) {
-                const float kk = sk[tt][rg + kRowGroups * j];
+                const float kk = f4_at(k4[j >> 2], j & 3);
                 s[j].x = __fmaf_rn(kk, d.x, s[j].x);
                 s[j].y = __fmaf_rn(kk, d.y, s[j].y);
                 s[j].z = __fmaf_rn(kk, d.z, s[j].z);
