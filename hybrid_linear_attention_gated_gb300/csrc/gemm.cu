@@ -9,6 +9,7 @@
 // problem size so that enough items exist to keep every SM streaming; from 32 tokens the
 // tcgen05 path (tc_gemm.cu) takes over.  Split partials are summed in a fixed slice
 // order, so results are deterministic.
+#include <cooperative_groups.h>
 #include <cstdlib>
 
 #include "common.cuh"
@@ -22,7 +23,10 @@ int router_split(int M, int Hd, int E);
 namespace {
 
 constexpr int kDenseThreads = 128;  // 4 warps, one item per warp
-constexpr int kNormThreads = 1024;  // RMSNorm kernels: one CTA per row (same layout => same sums)
+// RMSNorm kernels: one thread-block cluster of kNormCluster CTAs per row, each CTA a contiguous
+// eighth of the columns (same layout in both kernels => same sums)
+constexpr int kNormCluster = 8;
+constexpr int kNormThreads = 128;
 
 struct DenseParams {
     const uint16_t *W;
@@ -173,19 +177,6 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ part, int split, 
     }
 }
 
-// Fixed-order block sum (all threads get the result).  blockDim.x is a multiple of 32.
-__device__ float block_sum(float v, float *red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[w] = v;
-    __syncthreads();
-    float s = red[0];
-    for (int i = 1; i < nw; ++i) s = __fadd_rn(s, red[i]);
-    return s;
-}
-
 // o-projection epilogue fused with the next RMSNorm: r = (sum of split partials) + residual,
 // stored bf16, then xn = RMSNorm(r) * gamma.  Same thread layout and arithmetic order as
 // splitk_reduce_kernel followed by rmsnorm_kernel, so the results are bit-identical to them.
@@ -245,39 +236,70 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
                       pack_bf16x2(v[6], v[7]));
 }
 
-__global__ void __launch_bounds__(kNormThreads)
+// Fixed-order sum over one row's cluster (every thread gets the result): a warp butterfly,
+// the warps of a CTA in order, then the CTAs in rank order, read from their shared memory
+// through the cluster (distributed shared memory).
+__device__ float cluster_row_sum(float v, float *red) {
+    namespace cg = cooperative_groups;
+    constexpr int NW = kNormThreads / 32;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = red[0];
+        for (int i = 1; i < NW; ++i) s = __fadd_rn(s, red[i]);
+        red[NW] = s;
+    }
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();
+    float tot = *cl.map_shared_rank(&red[NW], 0);
+    for (int r = 1; r < kNormCluster; ++r) tot = __fadd_rn(tot, *cl.map_shared_rank(&red[NW], r));
+    cl.sync();  // every CTA has read the others' sums before any of them exits
+    return tot;
+}
+
+// Columns of a row handled by CTA `rank` of its cluster: 8-column groups [g0, g1).
+__device__ __forceinline__ void norm_range(int nv, int rank, int &g0, int &g1) {
+    const int per = (nv + kNormCluster - 1) / kNormCluster;
+    g0 = min(nv, rank * per);
+    g1 = min(nv, g0 + per);
+}
+
+__global__ void __launch_bounds__(kNormThreads) __cluster_dims__(kNormCluster, 1, 1)
     residual_rmsnorm_kernel(const float *__restrict__ part, int split, int M, int N,
-                                        const uint16_t *__restrict__ residual,
-                                        const uint16_t *__restrict__ gamma, float eps, uint16_t *r,
-                                        uint16_t *xn) {
-    __shared__ float red[32];
-    const int m = blockIdx.x;
+                            const uint16_t *__restrict__ residual,
+                            const uint16_t *__restrict__ gamma, float eps, uint16_t *r,
+                            uint16_t *xn) {
+    __shared__ float red[kNormThreads / 32 + 1];
+    const int m = blockIdx.x / kNormCluster;
     const size_t plane = (size_t)M * N;
     const float *pr = part + (size_t)m * N;
     uint4 *rr = reinterpret_cast<uint4 *>(r + (size_t)m * N);
     const uint4 *gr = reinterpret_cast<const uint4 *>(gamma);
     const uint4 *resr = residual ? reinterpret_cast<const uint4 *>(residual + (size_t)m * N) : nullptr;
     uint4 *yr = reinterpret_cast<uint4 *>(xn + (size_t)m * N);
-    const int nv = N / 8;
+    int g0, g1;
+    norm_range(N / 8, blockIdx.x % kNormCluster, g0, g1);
     float ss = 0.f;
-    if (nv <= (int)blockDim.x) {
-        const int i = threadIdx.x;
+    if (g1 - g0 <= kNormThreads) {
+        const int i = g0 + threadIdx.x;
         uint4 w = make_uint4(0, 0, 0, 0), gg = w, rw = w;
-        if (i < nv) {
+        if (i < g1) {
             if (resr) rw = ld_act_v4(resr + i);
             float v[8];
             residual_slices(pr, plane, split, i, resr != nullptr, rw, v);
-            gg = ld_act_v4(gr + i);  // in flight during the block reduction
+            gg = ld_act_v4(gr + i);  // in flight during the reduction
             w = pack8(v);
             rr[i] = w;
             ss = sum_squares8(w, ss);
         }
-        const float tot = block_sum(ss, red);
+        const float tot = cluster_row_sum(ss, red);
         const float inv = 1.0f / sqrtf(tot / (float)N + eps);
-        if (i < nv) yr[i] = scale8(w, gg, inv);
+        if (i < g1) yr[i] = scale8(w, gg, inv);
         return;
     }
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+    for (int i = g0 + threadIdx.x; i < g1; i += kNormThreads) {
         uint4 rw = make_uint4(0, 0, 0, 0);
         if (resr) rw = ld_act_v4(resr + i);
         float v[8];
@@ -286,9 +308,9 @@ __global__ void __launch_bounds__(kNormThreads)
         rr[i] = w;
         ss = sum_squares8(w, ss);
     }
-    const float tot = block_sum(ss, red);
+    const float tot = cluster_row_sum(ss, red);
     const float inv = 1.0f / sqrtf(tot / (float)N + eps);
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) yr[i] = scale8(rr[i], ld_act_v4(gr + i), inv);
+    for (int i = g0 + threadIdx.x; i < g1; i += kNormThreads) yr[i] = scale8(rr[i], ld_act_v4(gr + i), inv);
 }
 
 // Fixed-order block sum of two values at once (one pair of barriers instead of two).
@@ -344,34 +366,36 @@ __global__ void qkvg_epilogue_kernel(const float *__restrict__ part, int split, 
     if (i == 0) beta[(size_t)m * H + h] = 1.0f / (1.0f + expf(-zb));
 }
 
-// RMSNorm of bf16 rows, one CTA per row; thread layout and arithmetic order as in
+// RMSNorm of bf16 rows, one cluster per row; thread layout and arithmetic order as in
 // residual_rmsnorm_kernel's second half (x kept in registers when a thread owns one group).
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(int Hd, const uint16_t *__restrict__ x,
-                               const uint16_t *__restrict__ gamma, float eps, uint16_t *y) {
-    __shared__ float red[32];
-    const int m = blockIdx.x;
+__global__ void __launch_bounds__(kNormThreads) __cluster_dims__(kNormCluster, 1, 1)
+    rmsnorm_kernel(int Hd, const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
+                   float eps, uint16_t *y) {
+    __shared__ float red[kNormThreads / 32 + 1];
+    const int m = blockIdx.x / kNormCluster;
     const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)m * Hd);
     const uint4 *gr = reinterpret_cast<const uint4 *>(gamma);
     uint4 *yr = reinterpret_cast<uint4 *>(y + (size_t)m * Hd);
-    const int nv = Hd / 8;
+    int g0, g1;
+    norm_range(Hd / 8, blockIdx.x % kNormCluster, g0, g1);
     float ss = 0.f;
-    if (nv <= (int)blockDim.x) {
-        const int i = threadIdx.x;
+    if (g1 - g0 <= kNormThreads) {
+        const int i = g0 + threadIdx.x;
         uint4 w = make_uint4(0, 0, 0, 0), gg = w;
-        if (i < nv) {
+        if (i < g1) {
             w = ld_act_v4(xr + i);
             gg = ld_act_v4(gr + i);
             ss = sum_squares8(w, ss);
         }
-        const float tot = block_sum(ss, red);
+        const float tot = cluster_row_sum(ss, red);
         const float inv = 1.0f / sqrtf(tot / (float)Hd + eps);
-        if (i < nv) yr[i] = scale8(w, gg, inv);
+        if (i < g1) yr[i] = scale8(w, gg, inv);
         return;
     }
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) ss = sum_squares8(ld_act_v4(xr + i), ss);
-    const float tot = block_sum(ss, red);
+    for (int i = g0 + threadIdx.x; i < g1; i += kNormThreads) ss = sum_squares8(ld_act_v4(xr + i), ss);
+    const float tot = cluster_row_sum(ss, red);
     const float inv = 1.0f / sqrtf(tot / (float)Hd + eps);
-    for (int i = threadIdx.x; i < nv; i += blockDim.x)
+    for (int i = g0 + threadIdx.x; i < g1; i += kNormThreads)
         yr[i] = scale8(ld_act_v4(xr + i), ld_act_v4(gr + i), inv);
 }
 
@@ -579,7 +603,7 @@ int run_splitk_reduce(const float *part, int split, int M, int N, const hla_bf16
 
 int run_rmsnorm(int M, int Hd, const hla_bf16 *x, const hla_bf16 *gamma, float eps, hla_bf16 *y,
                 cudaStream_t st) {
-    rmsnorm_kernel<<<M, kNormThreads, 0, st>>>(Hd, x, gamma, eps, y);
+    rmsnorm_kernel<<<(unsigned)M * kNormCluster, kNormThreads, 0, st>>>(Hd, x, gamma, eps, y);
     return launch_status();
 }
 
@@ -745,7 +769,8 @@ extern "C" int skinny_proj_residual_rmsnorm(int M, int N, int K, const hla_bf16 
     float *part = reinterpret_cast<float *>(ws);
     int rc = run_dense(M, N, K, x, W, s, part, nullptr, 0, nullptr, st);
     if (rc != HLA_OK) return rc;
-    residual_rmsnorm_kernel<<<M, kNormThreads, 0, st>>>(part, s, M, N, residual, gamma, eps, r, xn);
+    residual_rmsnorm_kernel<<<(unsigned)M * kNormCluster, kNormThreads, 0, st>>>(part, s, M, N, residual,
+                                                                                 gamma, eps, r, xn);
     set_variant("proj_residual_rmsnorm<tt%d,split%d>", dense_tokens_per_tile(M), s);
     return launch_status();
 }
