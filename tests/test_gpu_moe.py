@@ -119,6 +119,30 @@ def test_proj_residual_rmsnorm(dev, M):
     assert frob_rel(f64(xn1), xn_ref) < PROJ_FROB_REL_BF16
 
 
+@pytest.mark.parametrize("M,N,K", [(2, 1032, 512), (3, 9216, 256), (1, 8, 64)])
+def test_proj_residual_rmsnorm_shapes(dev, M, N, K):
+    """The fused epilogue at widths that leave cluster CTAs partly or wholly empty and at a width
+    past 128 groups of 8 per CTA: bit-identical to the projection followed by hla_rmsnorm."""
+    g = inputs.generator(95 + N)
+    x, W = inputs.activations(M, K, g).to(dev), inputs.weight((N, K), g).to(dev)
+    res, gam = inputs.activations(M, N, g).to(dev), inputs.gains(N, g).to(dev)
+    r1 = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    xn1 = torch.empty_like(r1)
+    nb = hla.skinny_proj_residual_rmsnorm_workspace_size(M, N, K, 0)
+    ws = _ws(nb, dev)
+    hla.skinny_proj_residual_rmsnorm(M, N, K, x, W, res, gam, 1e-6, r1, xn1, 0, ws, nb)
+    split = int(hla.hla_last_variant().split("split")[1].rstrip(">"))
+    r2, xn2 = torch.empty_like(r1), torch.empty_like(r1)
+    ws2 = _ws(hla.skinny_proj_splitk_workspace_size(M, N, K, split), dev)
+    hla.skinny_proj_splitk(M, N, K, x, W, res, r2, hla.HLA_BF16, split, ws2, ws2.numel())
+    hla.hla_rmsnorm(M, N, r2, gam, 1e-6, xn2)
+    torch.cuda.synchronize()
+    assert torch.equal(r1, r2) and torch.equal(xn1, xn2)
+    r_ref = oracle.moe.linear(f64(x), f64(W)) + f64(res)
+    xn_ref = oracle.moe.rmsnorm(oracle.numerics.round_bf16(r_ref), f64(gam), 1e-6)
+    assert frob_rel(f64(xn1), xn_ref) < PROJ_FROB_REL_BF16
+
+
 def test_split_counts_agree(dev):
     M, N, K = 4, 512, 2048
     g = inputs.generator(3)
@@ -203,8 +227,11 @@ def test_qkvg_projection(dev, M, Hd, H, d):
     assert max_rel(f64(outs["beta"]), be) < 1e-4
 
 
-@pytest.mark.parametrize("M,Hd", [(1, 7168), (64, 7168), (3, 256)])
+@pytest.mark.parametrize("M,Hd", [(1, 7168), (64, 7168), (3, 256), (2, 8), (5, 40), (1, 8200),
+                                  (2, 16384)])
 def test_rmsnorm(dev, M, Hd):
+    """One thread-block cluster per row: rows narrower than the cluster (CTAs with no columns),
+    and rows wider than 128 groups of 8 per CTA (the looped path)."""
     g = inputs.generator(M + 5)
     x, gam = inputs.activations(M, Hd, g), inputs.gains(Hd, g)
     y = torch.empty(M, Hd, dtype=torch.bfloat16, device=dev)
