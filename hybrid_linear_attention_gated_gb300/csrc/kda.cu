@@ -267,13 +267,17 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
             d.y = __fmul_rn(bt, __fsub_rn(vv.y, u.y));
             d.z = __fmul_rn(bt, __fsub_rn(vv.z, u.z));
             d.w = __fmul_rn(bt, __fsub_rn(vv.w, u.w));
+            // the state after a verify program's last token is never read (no commit, and o comes
+            // from w, q.k and d): its update is skipped
+            if (COMMIT_END || t != steps - 1) {
 #pragma unroll
-            for (int j = 0; j < RPT; ++j) {
-                const float kk = f4_at(k4[j >> 2], j & 3);
-                s[j].x = __fmaf_rn(kk, d.x, s[j].x);
-                s[j].y = __fmaf_rn(kk, d.y, s[j].y);
-                s[j].z = __fmaf_rn(kk, d.z, s[j].z);
-                s[j].w = __fmaf_rn(kk, d.w, s[j].w);
+                for (int j = 0; j < RPT; ++j) {
+                    const float kk = f4_at(k4[j >> 2], j & 3);
+                    s[j].x = __fmaf_rn(kk, d.x, s[j].x);
+                    s[j].y = __fmaf_rn(kk, d.y, s[j].y);
+                    s[j].z = __fmaf_rn(kk, d.z, s[j].z);
+                    s[j].w = __fmaf_rn(kk, d.w, s[j].w);
+                }
             }
             if (WRITE_O && t >= n_pre && rg == 0) {
                 float4 o;
