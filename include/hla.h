@@ -207,7 +207,7 @@ int skinny_proj_splitk(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W
  *  xn = r * gamma / sqrt(mean(r^2) + eps)   over each row, stored bf16 [M, N]
  *  x bf16 [M, K]; W bf16 [N, K]; gamma bf16 [N]; K % 32 == 0, N % 8 == 0, 1 <= M <= 256.
  *  split as skinny_proj_splitk (0 = automatic; below 32 tokens the automatic split is at
- *  most 8, since the normalising pass sums every slice of a row in one CTA).  Bit-identical
+ *  most 8, since the normalising pass reads every slice of each of its columns).  Bit-identical
  *  to skinny_proj_splitk (bf16 output) followed by hla_rmsnorm with the same split.  The
  *  workspace holds the fp32 split partials (at least one slice).
  * -------------------------------------------------------------------------*/
