@@ -774,6 +774,24 @@ def run_profile(kind, iters=3):
         info.update(B=B, T=T, accepted=a.tolist(), verify_bytes=spec_bytes(B, T, a.cpu().numpy())["verify"],
                     replay_bytes=spec_bytes(B, T, a.cpu().numpy())["replay"],
                     variant=[verify_variant, hla.hla_last_variant()])
+    elif kind in ("layer1", "layer8"):
+        # the decode layer at batch 1 or 8 with the full-size weights: three warm-up calls, then
+        # `iters` calls in the NVTX range "timed" (for an ncu launch list of the small-batch layer)
+        M = 1 if kind == "layer1" else 8
+        wl = Workload(dev, 0)
+        x = inputs.activations(M, c["Hd"], g, dev)
+        S = wl.S[:M].clone()
+        y = torch.empty(M, c["Hd"], dtype=torch.bfloat16, device=dev)
+        nb = hla.hla_decode_layer_workspace_size(wl.L, M)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+
+        def layer_call(i):
+            hla.hla_decode_layer(wl.L, M, x, S, None, y, ws, nb, prefetch_stream=wl.side)
+        for i in range(3):
+            layer_call(i)
+        t = time_steps(torch, layer_call, iters, 1)
+        info.update(M=M, calls=iters, us_per_call_eager=round(t / iters * 1e6, 1),
+                    variant=hla.hla_last_variant())
     elif kind in ("dense", "dense16"):
         # the input projection at batch 64 (tensor-core path) or 16 (streaming path)
         M, H, d = (64 if kind == "dense" else 16), c["H"], c["d"]
@@ -917,7 +935,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true")
-    ap.add_argument("--profile", choices=["moe", "kda", "spec", "dense", "dense16"],
+    ap.add_argument("--profile", choices=["moe", "kda", "spec", "dense", "dense16", "layer1", "layer8"],
                     help="run one small case of a hot kernel (for ncu captures) and exit")
     ap.add_argument("--prefetch-ab", action="store_true",
                     help="time the layer under every side-stream prefetch mask and exit")
