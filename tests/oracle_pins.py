@@ -371,7 +371,59 @@ def layer_pin_failures(qkvg_epilogue, decode_layer, step, rmsnorm, round_bf16):
     S_ref, o_ref = step(S, qq, kq, vq, aq, bq)
     if not (np.allclose(S_new, S_ref, rtol=1e-14, atol=1e-14) and np.allclose(aux["o"], o_ref, rtol=1e-14, atol=1e-14)):
         fails.append("layer KDA composition")
+    fails += layer_worked_example_failures(decode_layer, round_bf16)
     return sorted(set(fails))
+
+
+def layer_worked_example_failures(decode_layer, round_bf16):
+    """The layer's second half (o-projection, residual, second RMSNorm, MoE input and the
+    residual after the experts) on the hand-worked example of golden/layer_worked_example.json.
+
+    Everything up to r is compared exactly with the hand-derived values.  x2 and y contain
+    a square root and exp, so they are re-derived here with scalar loops from the golden r
+    (math.sqrt, math.exp) and rounded with the separately pinned bf16 rounding; every value
+    lies at least 0.09 bf16 ulp away from a rounding tie, so float64 ordering cannot move
+    a rounding decision.
+    """
+    fails = []
+    ex = _load("layer_worked_example.json")
+    A = lambda v: np.array(v, dtype=float)  # noqa: E731
+    rows = ex["W_qkvgb_rows"]
+    W = A([rows[n] for n in ("q0", "q1", "k0", "k1", "v0", "v1", "g0", "g1", "beta")])
+    Hd = len(ex["x"])
+    p = dict(H=1, dk=2, dv=2, top_k=1, eps=1e-6, gamma_attn=A(ex["gamma_attn"]),
+             gamma_moe=A(ex["gamma_moe"]), W_qkvgb=W, W_o=A(ex["W_o"]), W_r=A(ex["W_r"]))
+    experts = (A(ex["W_gate"])[None], A(ex["W_up"])[None], A(ex["W_down"])[None])
+    x = A(ex["x"])[None]
+    S = A(ex["S"])[None, None]
+    y, S_new, aux = decode_layer(x, S, p, experts)
+    exact = dict(x1=(aux["x1"], ex["x1"]), q=(aux["q"], ex["q"]), k=(aux["k"], ex["k"]),
+                 v=(aux["v"], ex["v"]), alpha=(aux["alpha"], ex["alpha"]),
+                 beta=(aux["beta"], [ex["beta"]]), o=(aux["o"], ex["o"]), r=(aux["r"], ex["r"]),
+                 S_t=(S_new, ex["S_t"]))
+    for name, (got, want) in exact.items():
+        if np.size(got) != np.size(want) or not np.array_equal(np.ravel(got), np.ravel(A(want))):
+            fails.append(f"layer worked example {name}")
+
+    # x2 = bf16(RMSNorm(r) * gamma_moe), then the single routed expert (weight 1) and the
+    # residual r, in scalar loops
+    r = ex["r"]
+    inv = 1.0 / math.sqrt(sum(t * t for t in r) / Hd + 1e-6)
+    x2 = [float(round_bf16(np.float64(r[i] * inv * ex["gamma_moe"][i]))) for i in range(Hd)]
+    Wg, Wu, Wd = ex["W_gate"], ex["W_up"], ex["W_down"]
+    I = len(Wg)
+    g = [sum(Wg[i][j] * x2[j] for j in range(Hd)) for i in range(I)]
+    u = [sum(Wu[i][j] * x2[j] for j in range(Hd)) for i in range(I)]
+    h = [g[i] / (1.0 + math.exp(-g[i])) * u[i] for i in range(I)]
+    y_ref = [float(round_bf16(np.float64(r[i] + sum(Wd[i][j] * h[j] for j in range(I)))))
+             for i in range(Hd)]
+    if not np.array_equal(np.ravel(aux["x2"]), A(x2)):
+        fails.append("layer worked example x2 = RMSNorm(r)")
+    if np.shape(y) != (1, Hd) or not np.array_equal(np.ravel(y), A(y_ref)):
+        fails.append("layer worked example y = r + expert(x2)")
+    if not (np.array_equal(np.ravel(aux["topk_idx"]), [0]) and np.array_equal(np.ravel(aux["topk_w"]), [1.0])):
+        fails.append("layer worked example routing")
+    return fails
 
 
 # --------------------------------------------------------------------------------------

@@ -232,6 +232,43 @@ def test_layer_epilogue_mutants_are_caught(kind):
                    moe.rmsnorm, numerics.round_bf16)
 
 
+def _layer_variant(kind):
+    """A copy of the oracle's decode_layer with one plausible wiring mistake in its second half."""
+    rb = numerics.round_bf16
+
+    def decode_layer(x, S, p, experts, shared=()):
+        H, dk, dv, eps = p["H"], p["dk"], p["dv"], p.get("eps", 1e-6)
+        x = f64(x)
+        M = x.shape[0]
+        x1 = rb(moe.rmsnorm(x, p["gamma_attn"], eps))
+        q, k, v, alpha, beta = layer.qkvg_epilogue(moe.linear(x1, p["W_qkvgb"]), H, dk, dv)
+        S_new, o = kda.kda_step(S, q, k, v, alpha, beta)
+        o_b = (o if kind == "o_unrounded" else rb(o)).reshape(M, H * dv)
+        proj = f64(o_b) @ f64(p["W_o"]) if kind == "W_o_transposed" else moe.linear(o_b, p["W_o"])
+        r = rb(x + proj)
+        x2 = rb(moe.rmsnorm(r, p["gamma_moe"], eps))
+        idx, w, logits = moe.route_topk(x2, p["W_r"], p["top_k"])
+        moe_in = {"moe_fed_x1": x1, "moe_fed_x": x}.get(kind, x2)
+        res = x if kind == "residual_from_x" else r
+        y = rb(moe.moe_forward(moe_in, idx, w, experts, shared, residual=res))
+        aux = dict(x1=x1, q=q, k=k, v=v, alpha=alpha, beta=beta, o=o, r=r, x2=x2,
+                   topk_idx=idx, topk_w=w, logits=logits)
+        return y, S_new, aux
+    return decode_layer
+
+
+def test_layer_variant_without_mistake_passes():
+    assert layer_pin_failures(layer.qkvg_epilogue, _layer_variant("none"), kda.kda_step,
+                              moe.rmsnorm, numerics.round_bf16) == []
+
+
+@pytest.mark.parametrize("kind", ["W_o_transposed", "residual_from_x", "moe_fed_x1", "moe_fed_x",
+                                  "o_unrounded"])
+def test_layer_wiring_mutants_are_caught(kind):
+    assert _caught(layer_pin_failures, layer.qkvg_epilogue, _layer_variant(kind), kda.kda_step,
+                   moe.rmsnorm, numerics.round_bf16)
+
+
 def _fused_verifies_stale_state(S_c, prev, acc, new):
     S = kda.spec_replay(S_c, prev["q"], prev["k"], prev["v"], prev["alpha"], prev["beta"], acc)
     o = kda.spec_verify(S_c, new["q"], new["k"], new["v"], new["alpha"], new["beta"])
