@@ -31,6 +31,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -101,8 +102,7 @@ class ClockSampler:
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.gpu}.csv")
+            self.path = os.path.join(tempfile.mkdtemp(prefix="hla_clocks_"), f"clocks_rank{self.gpu}.csv")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
@@ -301,8 +301,8 @@ def kda_sweep(torch, hla, inputs, dev, peak):
                                 u["beta"], o)
         t = graph_time(torch, fn, iters)
         gbs = kda_bytes(B) / t / 1e9
-        res.append(dict(batch=B, us=round(t * 1e6, 2), gbs=round(gbs, 1), frac=round(gbs / peak, 3),
-                        variant=hla.hla_last_variant()))
+        res.append(dict(batch=B, us=round(t * 1e6, 2), tokens_per_s=round(B / t), gbs=round(gbs, 1),
+                        frac=round(gbs / peak, 3), variant=hla.hla_last_variant()))
     del pool
     return res
 
@@ -337,8 +337,8 @@ def moe_sweep(torch, hla, inputs, wl, dev, peak):
         U = statistics.mean(us)
         nbytes = layer_bytes(M, U)["router"] + layer_bytes(M, U)["experts"]
         gbs = nbytes / t / 1e9
-        res.append(dict(tokens=M, active_experts=U, us=round(t * 1e6, 1), gbs=round(gbs, 1),
-                        frac=round(gbs / peak, 3), variant=hla.hla_last_variant()))
+        res.append(dict(tokens=M, active_experts=U, us=round(t * 1e6, 1), tokens_per_s=round(M / t),
+                        gbs=round(gbs, 1), frac=round(gbs / peak, 3), variant=hla.hla_last_variant()))
     return res
 
 
@@ -376,20 +376,22 @@ def extend_sweep(torch, hla, inputs, dev, peak):
 
 
 def spec_sweep(torch, hla, inputs, wl, dev, peak):
-    """Speculative window, T=4, accepted length uniform in 0..4, at B=16 (33.5 MB of committed
-    state: fits in L2) and B=64 (134 MB: does not), two forms per step: separate (verify +
-    accept + replay) and fused (replay of the previous window with the verify of the next +
-    accept).  Each step rotates through 4 windows."""
+    """Speculative window, T=4, accepted length uniform in 0..4, at B=16 and B=64, two forms per
+    step: separate (verify + accept + replay) and fused (replay of the previous window with the
+    verify of the next + accept).  Each step takes the next B committed states of a 768 MB pool
+    (> 3x L2) through state_idx, so every step reads its states from HBM; the inputs rotate
+    through 4 windows.  tokens/s counts accepted tokens."""
     c = CFG
     T, H, d = c["spec_T"], c["H"], c["d"]
     tok = 3 * d * 2 + d * 4 + 4
+    pool_slots = 768 * 2 ** 20 // (H * d * d * 4)
+    pool = torch.randn(pool_slots, H, d, d, device=dev).mul_(0.05)
     res = []
     for B in (16, 64):
         if B == c["spec_B"]:
-            S, wins, ids = wl.S_spec.clone(), wl.win, wl.ids
+            wins, ids = wl.win, wl.ids
         else:
             g = inputs.generator(7700 + B, dev)
-            S = wl.S[:B].clone()
             wins, ids = [], []
             for _ in range(ROTATE):
                 wins.append(inputs.kda_inputs((B, T), H, d, d, g, dev))
@@ -398,20 +400,24 @@ def spec_sweep(torch, hla, inputs, wl, dev, peak):
         o = torch.empty(B, T, H, d, device=dev)
         acc = torch.zeros(B, dtype=torch.int32, device=dev)
         com = torch.zeros(B, dtype=torch.int32, device=dev)
+        iters = 4 * ROTATE
+        sets = pool_slots // B
+        idxs = [torch.arange((i % sets) * B, (i % sets + 1) * B, dtype=torch.int32, device=dev)
+                for i in range(iters)]
 
-        def separate(i, B=B, S=S, wins=wins, ids=ids, o=o, acc=acc, com=com):
+        def separate(i, B=B, wins=wins, ids=ids, o=o, acc=acc, com=com, idxs=idxs):
             w = wins[i % ROTATE]
             dr, tg, _ = ids[i % ROTATE]
-            hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, S, None, w["q"], w["k"],
+            hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, pool, idxs[i], w["q"], w["k"],
                                        w["v"], w["alpha"], w["beta"], None, o)
             hla.spec_accept_prefix(B, T, dr, tg, acc, com)
-            hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, S, None, w["q"], w["k"],
+            hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, pool, idxs[i], w["q"], w["k"],
                                        w["v"], w["alpha"], w["beta"], acc, None)
 
-        def fused(i, B=B, S=S, wins=wins, ids=ids, o=o, acc=acc, com=com):
+        def fused(i, B=B, wins=wins, ids=ids, o=o, acc=acc, com=com, idxs=idxs):
             p_, w = wins[(i + ROTATE - 1) % ROTATE], wins[i % ROTATE]
             dr, tg, _ = ids[i % ROTATE]
-            hla.kda_spec_replay_verify(B, T, T, H, d, d, S, None, p_["q"], p_["k"], p_["v"],
+            hla.kda_spec_replay_verify(B, T, T, H, d, d, pool, idxs[i], p_["q"], p_["k"], p_["v"],
                                        p_["alpha"], p_["beta"], acc, w["q"], w["k"], w["v"],
                                        w["alpha"], w["beta"], o)
             hla.spec_accept_prefix(B, T, dr, tg, acc, com)
@@ -419,10 +425,13 @@ def spec_sweep(torch, hla, inputs, wl, dev, peak):
         mean_fused = statistics.mean(
             B * H * 4 * d * d + sum(H * (4 * d * d + int(a) * tok) for a in ids[r][2] if a > 0)
             + B * H * T * (tok + 4 * d) + 2 * B * T * 4 + 3 * B * 4 for r in range(ROTATE))
+        accepted = statistics.mean(float(sum(ids[r][2])) for r in range(ROTATE))
         for name, fn, nbytes in (("separate", separate, mean_sep), ("fused", fused, mean_fused)):
-            t = graph_time(torch, fn, 4 * ROTATE)
+            t = graph_time(torch, fn, iters)
             res.append(dict(batch=B, form=name, us=round(t * 1e6, 2), bytes=round(nbytes),
+                            accepted_tokens=accepted, tokens_per_s=round(accepted / t),
                             gbs=round(nbytes / t / 1e9, 1), frac=round(nbytes / t / 1e9 / peak, 3)))
+    del pool
     return res
 
 
@@ -445,8 +454,8 @@ def layer_sweep(torch, hla, inputs, wl, dev, peak):
         U = int(torch.unique(ws[off:off + M * c["k"] * 4].view(torch.int32)).numel())
         nbytes = sum(layer_bytes(M, U).values())
         gbs = nbytes / t / 1e9
-        res.append(dict(batch=M, active_experts=U, us=round(t * 1e6, 1), gbs=round(gbs, 1),
-                        frac=round(gbs / peak, 3)))
+        res.append(dict(batch=M, active_experts=U, us=round(t * 1e6, 1), tokens_per_s=round(M / t),
+                        gbs=round(gbs, 1), frac=round(gbs / peak, 3)))
     return res
 
 
@@ -468,51 +477,36 @@ def traffic_entry(kernel, units):
     return dict(t, bytes_per_launch=round(t["per_unit_bytes"] * units))
 
 
-def cpu_baseline(wl, n_seq=8, reps=4):
-    """The fp64 oracle, as it stands, on a bounded sample of the step (host cores).  Its
-    inputs are handed over as float32 arrays (exact for bf16 values); the oracle upcasts
-    to float64 itself, as it always does.  The sample is timed ``reps`` times over (about
-    10 s of host work) so that the figure does not hang on one short measurement; the
-    weights the sample touches are brought to the host once, before the clock starts."""
-    import oracle
-    c = CFG
-    f = lambda t: t.detach().cpu().float().numpy()  # noqa: E731
-    p = dict(H=c["H"], dk=c["d"], dv=c["d"], top_k=c["k"], eps=c["eps"],
-             gamma_attn=f(wl.w["gamma_attn"]), gamma_moe=f(wl.w["gamma_moe"]),
-             W_qkvgb=f(wl.w["W_qkvgb"]), W_o=f(wl.w["W_o"]), W_r=f(wl.w["W_r"]))
-    x = f(wl.x[0][:n_seq])
-    S = f(wl.S[:n_seq])
-    cache = {}
-
-    def experts(e):
-        if e not in cache:
-            cache[e] = (f(wl.w["W_gate"][e]), f(wl.w["W_up"][e]), f(wl.w["W_down"][e]))
-        return cache[e]
-    shared = [(f(wl.w["Ws_gate"][0]), f(wl.w["Ws_up"][0]), f(wl.w["Ws_down"][0]))]
-    win = {k: f(v[:2]) for k, v in wl.win[0].items()}
-    S_spec = f(wl.S_spec[:2])
-    a = wl.ids[0][2][:2]
-
-    def sample():
-        used = set()
-        for m in range(n_seq):
-            _, _, aux = oracle.layer.decode_layer(x[m:m + 1], S[m:m + 1], p, experts, shared)
-            used.update(int(e) for e in aux["topk_idx"][0])
-        oracle.kda.spec_verify(S_spec, win["q"], win["k"], win["v"], win["alpha"], win["beta"])
-        oracle.kda.spec_replay(S_spec, win["q"], win["k"], win["v"], win["alpha"], win["beta"], a)
-        return used
-    sample()  # untimed: brings the sampled experts' weights to the host
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        used = sample()
-    dt = time.perf_counter() - t0
-    nbytes = sum(layer_bytes(n_seq, len(used)).values()) + sum(spec_bytes(2, c["spec_T"], a).values())
-    return dict(value=round(reps * nbytes / dt / 1e9, 4), unit="GB/s",
-                cores=len(os.sched_getaffinity(0)), kind="oracle", seconds=round(dt, 2),
-                sample=f"decode layer for {n_seq} of the 64 sequences (one at a time) + speculative "
-                       f"window for 2 of the 16 sequences, fp64 numpy oracle (inputs as fp32 host "
-                       f"arrays, upcast by the oracle), timed {reps} times over; bytes credited as "
-                       f"for that sample")
+def cpu_baseline(steps=3, warmup=3):
+    """The fp64 oracle, as it stands, on the host cores: the reference arm's bounded sample (per
+    step the decode layer for one of the 64 sequences and the speculative window for one of the
+    16), run in child processes with the BLAS / OpenMP thread pools limited to 1 thread and to
+    every core the process may use.  Reported beside the GPU number, not a target."""
+    cores = len(os.sched_getaffinity(0))
+    runs = {}
+    for threads in (cores, 1):
+        env = dict(os.environ)
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+            env[var] = str(threads)
+        cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--steps", str(steps),
+               "--warmup", str(warmup), "--threads", str(threads)]
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, cwd=ROOT)
+        line = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+        if r.returncode != 0 or not line:
+            runs[threads] = dict(error=(r.stderr or r.stdout)[-300:])
+            continue
+        runs[threads] = json.loads(line[-1])
+    best = runs.get(cores, {})
+    one = runs.get(1, {})
+    return dict(value=best.get("value"), unit="GB/s", cores=cores, kind="oracle",
+                ms_per_step=best.get("ms_per_step"),
+                single_thread=dict(value=one.get("value"), unit="GB/s", cores=1,
+                                   ms_per_step=one.get("ms_per_step")),
+                sample=(best.get("config") or {}).get("sample", "") +
+                f" ({steps} timed steps after {warmup} warm-up steps per thread count; weights drawn "
+                f"from the same distributions on the host; {os.uname().machine}, {cores} cores)",
+                **({"errors": {k: v["error"] for k, v in runs.items() if "error" in v}}
+                   if any("error" in v for v in runs.values()) else {}))
 
 
 def run_ours(args):
@@ -535,6 +529,10 @@ def run_ours(args):
 
     sampler = ClockSampler(local)
     sampler.start()
+    # the states as they enter the timed region: the same steps are replayed from them afterwards
+    # to read each timed step's routing (the kernels are deterministic, so the replay takes the
+    # same routing decisions; its final states are checked bit for bit against the timed run's)
+    snap = [t.clone() for t in (wl.S, wl.S_spec, wl.acc, wl.com)]
     hla.hla_trace_enable("moe_gateup", args.steps)
     n0 = hla.hla_launch_count()
     elapsed = time_steps(torch, wl.step, args.steps, world)
@@ -542,18 +540,27 @@ def run_ours(args):
     gu_ms = hla.hla_trace_read(args.steps)
     hla.hla_trace_enable(None, 0)
 
-    # active experts of the routed steps (routing depends on the evolving state: sample a few)
+    # active experts of every timed step, from the deterministic replay
+    final = [t.clone() for t in (wl.S, wl.S_spec, wl.acc, wl.com)]
+    for t, s0 in zip((wl.S, wl.S_spec, wl.acc, wl.com), snap):
+        t.copy_(s0)
     Us = []
-    for i in range(ROTATE):
+    for i in range(args.steps):
         wl.step(i)
         torch.cuda.synchronize()
         Us.append(wl.active_experts())
+    replay_bitwise = all(torch.equal(a, b) for a, b in zip((wl.S, wl.S_spec, wl.acc, wl.com), final))
+    del snap, final
     U = statistics.mean(Us)
+    layer_total = sum(sum(layer_bytes(c["M"], u).values()) for u in Us)
     per_step = layer_bytes(c["M"], U)
     accepted = [wl.ids[i % ROTATE][2] for i in range(args.steps)]
     spec_total = sum(sum(spec_bytes(c["spec_B"], c["spec_T"], a).values()) for a in accepted)
-    local_bytes = sum(per_step.values()) * args.steps + spec_total
+    local_bytes = layer_total + spec_total
+    # tokens a step advances: one per decoding sequence, plus the accepted drafted tokens
+    local_tokens = c["M"] * args.steps + sum(int(sum(a)) for a in accepted)
     t_max, all_bytes = reduce_over_ranks(elapsed, local_bytes, world)
+    _, all_tokens = reduce_over_ranks(elapsed, local_tokens, world)
 
     # end to end through host buffers: pinned host inputs in, results out, every step.  A step's
     # inputs sit in one pinned buffer and go over in one copy (the library reads them through
@@ -655,8 +662,9 @@ def run_ours(args):
         return
     value = all_bytes / t_max / 1e9
     gu_avg_s = statistics.mean(gu_ms) / 1e3 if gu_ms else None
-    gu_b = gateup_bytes(c["M"], U)
-    achieved = gu_b / gu_avg_s / 1e9 if gu_avg_s else None
+    # the gate/up launches timed above, each with its own step's routing
+    gu_b = statistics.mean(gateup_bytes(c["M"], u) for u in Us[:len(gu_ms)]) if gu_ms else gateup_bytes(c["M"], U)
+    achieved = gu_b / gu_avg_s / 1e9 if gu_avg_s else None  # bytes per launch / mean launch time
     tr = traffic_entry("moe_gateup_kernel", U + c["n_shared"])
     out = {
         "metric": METRIC,
@@ -667,6 +675,9 @@ def run_ours(args):
         "warmup": args.warmup,
         "ms_per_step": round(t_max / args.steps * 1e3, 4),
         "us_per_step": round(t_max / args.steps * 1e6, 1),
+        "tokens_per_s": round(all_tokens / t_max),
+        "tokens_note": "tokens advanced per step: one per decoding sequence of the layer (64) plus "
+                       "the accepted drafted tokens of the speculative window",
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -678,7 +689,9 @@ def run_ours(args):
                         "state; 256 routed experts top-8 + 1 shared, intermediate 2048; L2 prefetch "
                         "on a side stream) + speculative window B=16, T=4 (verify, accept, replay)",
             "batch": c["M"], "spec_batch": c["spec_B"], "draft_len": c["spec_T"],
-            "active_experts_mean": U, "active_experts_samples": Us,
+            "active_experts_mean": U, "active_experts_per_timed_step": Us,
+            "routing_from": "a deterministic replay of the timed steps from their starting states "
+                            f"(final states bit-identical to the timed run: {replay_bitwise})",
             "bytes_per_step": round(local_bytes / args.steps),
             "l2": "working set ~20 GB per step >> 129 MB L2 (inputs larger than L2; no flush)",
             "parallelism": f"replicas x{world} (no collective on the data path)",
@@ -709,7 +722,7 @@ def run_ours(args):
         "sweeps": sweeps,
     }
     if not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(wl)
+        out["cpu_baseline"] = cpu_baseline()
     print(json.dumps(out))
 
 
@@ -850,6 +863,47 @@ def run_prefetch_ab(reps=4):
                                "during dispatch; 4 = shared down"}))
 
 
+# ----------------------------------------------------------------------------- layer A/B
+
+def run_layer_ab(spec, reps=5, batches=(1, 2, 8, 32, 64)):
+    """Layer time (CUDA graph of 8 calls, with the prefetch stream) at several batch sizes for
+    each value of one tuning switch, e.g. ``HLA_PDL=0,1``; repetitions are interleaved so that
+    the values see the same clocks.  One JSON line with the medians and the clocks."""
+    import torch
+    from hybrid_linear_attention_gated_gb300 import build, hla, inputs
+    var, vals = spec.split("=")
+    vals = vals.split(",")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    wl = Workload(dev, 0, prefetch=True)
+    c = CFG
+    sampler = ClockSampler(0)
+    sampler.start()
+    table = {}
+    for M in batches:
+        g = inputs.generator(9000 + M, dev)
+        xs = [inputs.activations(M, c["Hd"], g, dev) for _ in range(ROTATE)]
+        S = wl.S[:M].clone() if M <= c["M"] else None
+        if S is None:
+            continue
+        y = torch.empty(M, c["Hd"], dtype=torch.bfloat16, device=dev)
+        nb = hla.hla_decode_layer_workspace_size(wl.L, M)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        res = {v: [] for v in vals}
+        for _ in range(reps):
+            for v in vals:
+                os.environ[var] = v
+
+                def fn(i):
+                    hla.hla_decode_layer(wl.L, M, xs[i % ROTATE], S, None, y, ws, nb, prefetch_stream=wl.side)
+                res[v].append(graph_time(torch, fn, 8) * 1e6)
+        os.environ.pop(var, None)
+        table[M] = {v: round(statistics.median(t), 2) for v, t in res.items()}
+    clocks = sampler.stop()
+    print(json.dumps({"layer_ab_us_per_call": table, "switch": var, "reps": reps, "clocks": clocks}))
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -862,6 +916,8 @@ def run_reference(args):
     import numpy as np
     import torch
     import oracle
+    if args.threads > 0:
+        torch.set_num_threads(args.threads)
     from hybrid_linear_attention_gated_gb300 import inputs
     c = CFG
     f = lambda t: t.float().numpy()  # noqa: E731  (exact for bf16; the oracle upcasts)
@@ -908,7 +964,7 @@ def run_reference(args):
     nbytes = sum(one(i) for i in range(args.steps))
     dt = time.perf_counter() - t0
     value = nbytes / dt / 1e9
-    cores = len(os.sched_getaffinity(0))
+    cores = args.threads if args.threads > 0 else len(os.sched_getaffinity(0))
     sample = ("per step: the decode layer for 1 of the 64 sequences and the speculative window "
               "for 1 of the 16 sequences, fp64 numpy oracle; bytes credited as for that sample")
     print(json.dumps({
@@ -935,15 +991,22 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true")
+    ap.add_argument("--threads", type=int, default=0,
+                    help="reference arm: host threads the oracle may use (0 = every core); the "
+                         "BLAS thread count is fixed by its environment variables at start-up")
     ap.add_argument("--profile", choices=["moe", "kda", "spec", "dense", "dense16", "layer1", "layer8"],
                     help="run one small case of a hot kernel (for ncu captures) and exit")
     ap.add_argument("--prefetch-ab", action="store_true",
                     help="time the layer under every side-stream prefetch mask and exit")
+    ap.add_argument("--layer-ab", metavar="VAR=v1,v2",
+                    help="time the layer at batch 1-64 for each value of one tuning switch and exit")
     args = ap.parse_args()
     if args.profile:
         return run_profile(args.profile)
     if args.prefetch_ab:
         return run_prefetch_ab()
+    if args.layer_ab:
+        return run_layer_ab(args.layer_ab)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

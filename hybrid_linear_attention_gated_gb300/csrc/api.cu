@@ -43,6 +43,23 @@ void trace_after(int kernel, cudaStream_t st) {
     ++g_trace.count;
 }
 
+namespace {
+thread_local bool g_pdl_on = false;
+thread_local cudaStream_t g_pdl_stream = nullptr;
+}  // namespace
+
+PdlChain::PdlChain(cudaStream_t st, bool on) : prev_on(g_pdl_on), prev_st(g_pdl_stream) {
+    g_pdl_on = on;
+    g_pdl_stream = st;
+}
+
+PdlChain::~PdlChain() {
+    g_pdl_on = prev_on;
+    g_pdl_stream = prev_st;
+}
+
+bool pdl_for(cudaStream_t st) { return g_pdl_on && st == g_pdl_stream; }
+
 int prefetch_mask() {
     const char *env = getenv("HLA_PREFETCH_MASK");
     return env ? (atoi(env) & 7) : -1;

@@ -27,6 +27,15 @@ inline int launch_status() {
     return HLA_OK;
 }
 
+// Status of a launch made through launch_kernel (its error is also consumed from the runtime).
+inline int launched(cudaError_t e) {
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return HLA_ERR_CUDA;
+    }
+    return launch_status();
+}
+
 // Optional per-kernel event timing (see hla_trace_enable).
 enum TraceKernel { kTraceNone = 0, kTraceKda, kTraceDense, kTraceMoeGateup, kTraceMoeDown };
 void trace_before(int kernel, cudaStream_t st);
@@ -43,6 +52,39 @@ int sm_count();
 // kPrefetchSharedGateUp / kPrefetchSharedDown: the shared experts' weights during dispatch.
 enum { kPrefetchLayer = 1, kPrefetchSharedGateUp = 2, kPrefetchSharedDown = 4 };
 int prefetch_mask();
+
+// ----------------------------------------------------------------------------- launch chains
+// Programmatic dependent launch.  Inside a chain (the decode layer's main stream, see
+// PdlChain) every kernel after the first is launched with programmatic stream serialisation:
+// it may start while its predecessor still runs, does the work that does not depend on the
+// predecessor (e.g. loading static weights or its own state), then waits (pdl_wait) until the
+// predecessor has completed and its writes are visible.  Each kernel lets its successor start
+// (pdl_trigger) only after its own wait, so when a kernel starts, every kernel before its
+// immediate predecessor has completed: its pre-wait reads may touch anything the immediate
+// predecessor does not write.  Outside a chain every launch is plain and pdl_wait is a no-op.
+struct PdlChain {
+    PdlChain(cudaStream_t st, bool on);
+    ~PdlChain();
+    bool prev_on;
+    cudaStream_t prev_st;
+};
+bool pdl_for(cudaStream_t st);  // launch with programmatic serialisation on this stream?
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_for(st) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 #define HLA_REQUIRE(cond, status) \
     do {                          \
@@ -91,6 +133,15 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Wait for the stream predecessor of a programmatically launched kernel (no-op otherwise), then
+// let this kernel's own successor start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_trigger() {
+    pdl_wait();
+    pdl_trigger();
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }

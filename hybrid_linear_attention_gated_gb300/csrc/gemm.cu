@@ -20,6 +20,17 @@ namespace hla {
 int dense_auto_split(int M, int N, int K);   // shared with the layer executor
 int router_split(int M, int Hd, int E);
 
+// HLA_DENSE_XITEM=0 keeps one item per warp on the streaming path (A/B runs).
+bool dense_cross_item() {
+    const char *env = getenv("HLA_DENSE_XITEM");
+    return !(env && env[0] == '0');
+}
+
+// The streaming path's persistent cross-item kernel applies (else one item per warp).
+bool dense_xi_applies(int N, int K, int split) {
+    return N % 32 == 0 && min_slice_steps(K, split) >= 4 && dense_cross_item();
+}
+
 namespace {
 
 constexpr int kDenseThreads = 128;  // 4 warps, one item per warp
@@ -71,7 +82,8 @@ __global__ void __launch_bounds__(kDenseThreads) dense_stream_kernel(const Dense
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[h][nt][e] = 0.f;
-    warp_stream_tile<2, NT, UNROLL>(wg, wg8, xr, kb, ke, acc);
+    // the weights are static: their first loads go out before waiting for the tokens
+    warp_stream_tile<2, NT, UNROLL>(wg, wg8, xr, kb, ke, acc, [] { pdl_wait_trigger(); });
 
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -158,12 +170,15 @@ __global__ void __launch_bounds__(kDenseThreads, dense_xi_min_blocks(NT))
         }
     };
     StridedClaims claims{warp, nwarps};
-    stream_items<2, NT, 4, DenseCtx>(claims, total, (size_t)8 * p.K, decode, epilogue);
+    // the weights are static: the first ring's weight loads go out before waiting for the tokens
+    stream_items<2, NT, 4, DenseCtx>(claims, total, (size_t)8 * p.K, decode, epilogue,
+                                     [] { pdl_wait_trigger(); });
 }
 
 // y = sum over slices in increasing order (+ residual)
 __global__ void splitk_reduce_kernel(const float *__restrict__ part, int split, int M, int N,
                                      const uint16_t *__restrict__ residual, void *y, int y_bf16) {
+    pdl_wait_trigger();
     const size_t total = (size_t)M * N;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
@@ -285,11 +300,16 @@ __global__ void __launch_bounds__(kNormThreads) __cluster_dims__(kNormCluster, 1
     if (g1 - g0 <= kNormThreads) {
         const int i = g0 + threadIdx.x;
         uint4 w = make_uint4(0, 0, 0, 0), gg = w, rw = w;
+        // gamma and the residual do not come from the projection before this kernel: loaded
+        // before waiting for it
         if (i < g1) {
             if (resr) rw = ld_act_v4(resr + i);
+            gg = ld_act_v4(gr + i);
+        }
+        pdl_wait_trigger();
+        if (i < g1) {
             float v[8];
             residual_slices(pr, plane, split, i, resr != nullptr, rw, v);
-            gg = ld_act_v4(gr + i);  // in flight during the reduction
             w = pack8(v);
             rr[i] = w;
             ss = sum_squares8(w, ss);
@@ -299,6 +319,7 @@ __global__ void __launch_bounds__(kNormThreads) __cluster_dims__(kNormCluster, 1
         if (i < g1) yr[i] = scale8(w, gg, inv);
         return;
     }
+    pdl_wait_trigger();
     for (int i = g0 + threadIdx.x; i < g1; i += kNormThreads) {
         uint4 rw = make_uint4(0, 0, 0, 0);
         if (resr) rw = ld_act_v4(resr + i);
@@ -340,6 +361,7 @@ __global__ void qkvg_epilogue_kernel(const float *__restrict__ part, int split, 
                                      uint16_t *q, uint16_t *k, uint16_t *v, float *alpha,
                                      float *beta) {
     __shared__ float2 red[32];
+    pdl_wait_trigger();
     const int m = blockIdx.x / H, h = blockIdx.x % H, i = threadIdx.x;
     const int Nq = 4 * H * d + H;
     const size_t plane = (size_t)M * Nq;
@@ -382,9 +404,10 @@ __global__ void __launch_bounds__(kNormThreads) __cluster_dims__(kNormCluster, 1
     if (g1 - g0 <= kNormThreads) {
         const int i = g0 + threadIdx.x;
         uint4 w = make_uint4(0, 0, 0, 0), gg = w;
+        if (i < g1) gg = ld_act_v4(gr + i);  // static: before the wait
+        pdl_wait_trigger();
         if (i < g1) {
             w = ld_act_v4(xr + i);
-            gg = ld_act_v4(gr + i);
             ss = sum_squares8(w, ss);
         }
         const float tot = cluster_row_sum(ss, red);
@@ -392,6 +415,7 @@ __global__ void __launch_bounds__(kNormThreads) __cluster_dims__(kNormCluster, 1
         if (i < g1) yr[i] = scale8(w, gg, inv);
         return;
     }
+    pdl_wait_trigger();
     for (int i = g0 + threadIdx.x; i < g1; i += kNormThreads) ss = sum_squares8(ld_act_v4(xr + i), ss);
     const float tot = cluster_row_sum(ss, red);
     const float inv = 1.0f / sqrtf(tot / (float)Hd + eps);
@@ -402,17 +426,18 @@ __global__ void __launch_bounds__(kNormThreads) __cluster_dims__(kNormCluster, 1
 // One CTA per token.  The split partials of the fp32 logits are summed by all 1024 threads:
 // each expert's slices are cut into nq = 1024 / E contiguous chunks, a thread sums one chunk
 // in increasing slice order with eight loads in flight, and the chunk sums are added in
-// chunk order (a fixed order, independent of the GPU).  Then one warp picks the top k on the
-// logits (ties to the lower index), takes sigmoid scores of the chosen experts and
-// renormalises them.
+// chunk order (a fixed order, independent of the GPU).  Then every expert's thread finds its
+// rank on the logits (ties to the lower index) in one pass; the k first are the top k, whose
+// sigmoid scores one thread renormalises.
 constexpr int kRouterThreads = 1024;
 
 __global__ void __launch_bounds__(kRouterThreads)
     router_topk_kernel(const float *__restrict__ part, int split, int M, int E, int k,
                        int32_t *topk_idx, float *topk_w, float *logits_out) {
-    __shared__ float lg[1024];
+    __shared__ __align__(16) float lg[1024];
     __shared__ float chunk[kRouterThreads];
     __shared__ float sel[16];
+    pdl_wait_trigger();
     const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
     const size_t plane = (size_t)M * E;
     const int nq = kRouterThreads / E;  // E <= 1024
@@ -446,27 +471,26 @@ __global__ void __launch_bounds__(kRouterThreads)
         if (logits_out) logits_out[(size_t)m * E + tid] = s;
     }
     __syncthreads();
-    if (tid >= 32) return;
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
-        for (int e = lane; e < E; e += 32) {
-            const float v = lg[e];
-            if (v > bv || (v == bv && e < be)) { bv = v; be = e; }
+    // Selection by rank: expert e's place in the order (logit descending, index ascending) is the
+    // number of experts ahead of it; the k experts with rank < k are the top k, listed by rank.
+    // Every thread reads the same logit at a time (a shared-memory broadcast).
+    if (tid < E) {
+        const float v = lg[tid];
+        int rank = 0;
+        const int E4 = E & ~3;
+        for (int e = 0; e < E4; e += 4) {
+            const float4 o = *reinterpret_cast<const float4 *>(&lg[e]);
+            rank += (o.x > v || (o.x == v && e < tid)) + (o.y > v || (o.y == v && e + 1 < tid)) +
+                    (o.z > v || (o.z == v && e + 2 < tid)) + (o.w > v || (o.w == v && e + 3 < tid));
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        for (int e = E4; e < E; ++e) rank += lg[e] > v || (lg[e] == v && e < tid);
+        if (rank < k) {
+            topk_idx[(size_t)m * k + rank] = tid;
+            sel[rank] = v;
         }
-        if (lane == 0) {
-            topk_idx[(size_t)m * k + j] = be;
-            sel[j] = bv;
-            lg[be] = -INFINITY;
-        }
-        __syncwarp();
     }
+    __syncthreads();
+    if (tid >= 32) return;
     if (lane == 0) {
         float sc[16], tot = 0.f;
 #pragma unroll
@@ -495,20 +519,10 @@ __global__ void l2_prefetch_kernel(const char *p, size_t bytes, uint32_t chunk) 
     }
 }
 
-// HLA_DENSE_XITEM=0 keeps one item per warp on the streaming path (A/B runs).
-bool dense_cross_item() {
-    const char *env = getenv("HLA_DENSE_XITEM");
-    return !(env && env[0] == '0');
-}
-
-// The streaming path's persistent cross-item kernel applies (else one item per warp).
-bool dense_xi_applies(int N, int K, int split) {
-    return N % 32 == 0 && min_slice_steps(K, split) >= 4 && dense_cross_item();
-}
-
 template <int NT>
 int launch_dense_nt(const DenseParams &p, cudaStream_t st) {
     const long items = (long)((p.N + 31) / 32) * p.split * p.ntg;
+    cudaError_t e;
     trace_before(kTraceDense, st);
     if (dense_xi_applies(p.N, p.K, p.split)) {
         // as many warps as keep every warp at the same item count within the resident set
@@ -525,13 +539,14 @@ int launch_dense_nt(const DenseParams &p, cudaStream_t st) {
         const long per_warp = (items + res - 1) / res;
         const long nwarps = (items + per_warp - 1) / per_warp;
         const long blocks = (nwarps * 32 + kDenseThreads - 1) / kDenseThreads;
-        dense_stream_xi_kernel<NT><<<(unsigned)blocks, kDenseThreads, 0, st>>>(p, (int)nwarps);
+        e = launch_kernel(dense_stream_xi_kernel<NT>, dim3((unsigned)blocks), dim3(kDenseThreads), 0, st,
+                          p, (int)nwarps);
     } else {
         const long blocks = (items * 32 + kDenseThreads - 1) / kDenseThreads;
-        dense_stream_kernel<NT, 4><<<(unsigned)blocks, kDenseThreads, 0, st>>>(p);
+        e = launch_kernel(dense_stream_kernel<NT, 4>, dim3((unsigned)blocks), dim3(kDenseThreads), 0, st, p);
     }
     trace_after(kTraceDense, st);
-    return launch_status();
+    return launched(e);
 }
 
 }  // namespace
@@ -597,14 +612,15 @@ int run_splitk_reduce(const float *part, int split, int M, int N, const hla_bf16
     const int threads = 256;
     long blocks = (long)((total + threads - 1) / threads);
     if (blocks > 8L * sm_count()) blocks = 8L * sm_count();
-    splitk_reduce_kernel<<<(unsigned)blocks, threads, 0, st>>>(part, split, M, N, residual, y, y_bf16);
-    return launch_status();
+    return launched(launch_kernel(splitk_reduce_kernel, dim3((unsigned)blocks), dim3(threads), 0, st,
+                                  part, split, M, N, reinterpret_cast<const uint16_t *>(residual), y, y_bf16));
 }
 
 int run_rmsnorm(int M, int Hd, const hla_bf16 *x, const hla_bf16 *gamma, float eps, hla_bf16 *y,
                 cudaStream_t st) {
-    rmsnorm_kernel<<<(unsigned)M * kNormCluster, kNormThreads, 0, st>>>(Hd, x, gamma, eps, y);
-    return launch_status();
+    return launched(launch_kernel(rmsnorm_kernel, dim3((unsigned)M * kNormCluster), dim3(kNormThreads), 0,
+                                  st, Hd, reinterpret_cast<const uint16_t *>(x),
+                                  reinterpret_cast<const uint16_t *>(gamma), eps, reinterpret_cast<uint16_t *>(y)));
 }
 
 int run_l2_prefetch(const void *ptr, size_t bytes, cudaStream_t st) {
@@ -623,8 +639,9 @@ int run_qkvg(int M, int Hd, int H, int d, const hla_bf16 *x, const hla_bf16 *W, 
     const int Nq = 4 * H * d + H;
     int s = run_dense(M, Nq, Hd, x, W, split, part, nullptr, 0, nullptr, st);
     if (s != HLA_OK) return s;
-    qkvg_epilogue_kernel<<<M * H, d, 0, st>>>(part, split, M, H, d, q, k, v, alpha, beta);
-    return launch_status();
+    return launched(launch_kernel(qkvg_epilogue_kernel, dim3(M * H), dim3(d), 0, st, (const float *)part,
+                                  split, M, H, d, reinterpret_cast<uint16_t *>(q), reinterpret_cast<uint16_t *>(k),
+                                  reinterpret_cast<uint16_t *>(v), alpha, beta));
 }
 
 int run_router(int M, int Hd, int E, int k, const hla_bf16 *x, const hla_bf16 *W_r, int32_t *idx,
@@ -632,8 +649,8 @@ int run_router(int M, int Hd, int E, int k, const hla_bf16 *x, const hla_bf16 *W
     const int split = router_split(M, Hd, E);
     int s = run_dense(M, E, Hd, x, W_r, split, part, nullptr, 0, nullptr, st);
     if (s != HLA_OK) return s;
-    router_topk_kernel<<<M, kRouterThreads, 0, st>>>(part, split, M, E, k, idx, w, logits);
-    return launch_status();
+    return launched(launch_kernel(router_topk_kernel, dim3(M), dim3(kRouterThreads), 0, st, (const float *)part,
+                                  split, M, E, k, idx, w, logits));
 }
 
 }  // namespace hla
@@ -769,8 +786,10 @@ extern "C" int skinny_proj_residual_rmsnorm(int M, int N, int K, const hla_bf16 
     float *part = reinterpret_cast<float *>(ws);
     int rc = run_dense(M, N, K, x, W, s, part, nullptr, 0, nullptr, st);
     if (rc != HLA_OK) return rc;
-    residual_rmsnorm_kernel<<<(unsigned)M * kNormCluster, kNormThreads, 0, st>>>(part, s, M, N, residual,
-                                                                                 gamma, eps, r, xn);
+    const cudaError_t e = launch_kernel(
+        residual_rmsnorm_kernel, dim3((unsigned)M * kNormCluster), dim3(kNormThreads), 0, st, (const float *)part, s,
+        M, N, reinterpret_cast<const uint16_t *>(residual), reinterpret_cast<const uint16_t *>(gamma), eps,
+        reinterpret_cast<uint16_t *>(r), reinterpret_cast<uint16_t *>(xn));
     set_variant("proj_residual_rmsnorm<tt%d,split%d>", dense_tokens_per_tile(M), s);
-    return launch_status();
+    return launched(e);
 }

@@ -59,8 +59,16 @@ struct KdaParams {
 // Tokens are staged through shared memory in blocks of TMAX; the state stays in registers
 // for the whole program.  Every step is the same arithmetic, so any combination is
 // bit-identical to the corresponding sequence of single steps.
+// The multi-token verify programs are held to 128 registers per thread (4 CTAs of 128 threads,
+// or 16 one-warp CTAs, per SM); left free they take up to 146 and lose a resident CTA.  The
+// other programs stay near 128 on their own (decode, replay) or spill under the cap (extend),
+// so they get no minimum (0: the compiler's own choice, as with no second bound).
+constexpr int kda_min_blocks(int cw, int mode) {
+    return (mode == 1 || mode == 3) ? 65536 / (kRowGroups * cw / 4 * 128) : 0;
+}
+
 template <int DK, int CW, int MODE>
-__global__ void __launch_bounds__(kRowGroups *CW / 4)
+__global__ void __launch_bounds__(kRowGroups *CW / 4, kda_min_blocks(CW, MODE))
     kda_recur_kernel(const KdaParams p) {
     constexpr int CG = CW / 4;
     constexpr int RPT = DK / kRowGroups;
@@ -91,6 +99,12 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
     const int h = bh % p.H;
     const int b = bh / p.H;
     const int col0 = slice * CW;
+
+    // Decode and verify read their state slice before waiting for the kernel before them (in a
+    // launch chain that kernel produces the tokens, never the state); the other programs first
+    // read accepted lengths or sequence offsets, which the kernel before them may write.
+    constexpr bool STATE_FIRST = MODE == kDecode || MODE == kVerify;
+    if (!STATE_FIRST) pdl_wait_trigger();
 
     int n_pre = 0, n_main = MODE == kDecode ? 1 : p.T;
     int seq0 = 0;
@@ -124,10 +138,23 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
     const int slot = p.state_idx ? p.state_idx[b] : b;
     float *Sb = p.S + ((size_t)slot * p.H + h) * (size_t)(DK * DV) + col0 + cg * 4;
 
-    float4 s[RPT];
+    // the thread's 4 columns as two float2 pairs (columns 0-1, 2-3), so that the per-row
+    // arithmetic runs as packed fp32x2 operations: two correctly rounded fp32 results per
+    // instruction, the same bits as two scalar operations
+    float2 s[RPT][2];
 #pragma unroll
-    for (int j = 0; j < RPT; ++j)
-        s[j] = *reinterpret_cast<const float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV);
+    for (int j = 0; j < RPT; ++j) {
+        const float4 t = *reinterpret_cast<const float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV);
+        s[j][0] = make_float2(t.x, t.y);
+        s[j][1] = make_float2(t.z, t.w);
+    }
+    auto store_state = [&]() {
+#pragma unroll
+        for (int j = 0; j < RPT; ++j)
+            *reinterpret_cast<float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV) =
+                make_float4(s[j][0].x, s[j][0].y, s[j][1].x, s[j][1].y);
+    };
+    if (STATE_FIRST) pdl_wait_trigger();
 
     // Only extend programs can exceed one block of TMAX tokens; for the others the loop body
     // runs once with every step in it (and compiles to straight-line code).
@@ -221,7 +248,7 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
 
         for (int tt = 0; tt < tn; ++tt) {
             const int t = t0 + tt;
-            float4 pu = make_float4(0.f, 0.f, 0.f, 0.f), pw = pu;
+            float2 pu[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, pw[2] = {pu[0], pu[1]};
             float pqk = 0.f;
             const float4 *a4 = reinterpret_cast<const float4 *>(&sa[tt][rg * PAD]);
             const float4 *k4 = reinterpret_cast<const float4 *>(&sk[tt][rg * PAD]);
@@ -230,97 +257,80 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4)
             for (int j = 0; j < RPT; ++j) {  // row rg + 8 j
                 const float a = f4_at(a4[j >> 2], j & 3), kk = f4_at(k4[j >> 2], j & 3),
                             qq = f4_at(q4[j >> 2], j & 3);
-                s[j].x = __fmul_rn(s[j].x, a);
-                s[j].y = __fmul_rn(s[j].y, a);
-                s[j].z = __fmul_rn(s[j].z, a);
-                s[j].w = __fmul_rn(s[j].w, a);
-                pu.x = __fmaf_rn(kk, s[j].x, pu.x);
-                pu.y = __fmaf_rn(kk, s[j].y, pu.y);
-                pu.z = __fmaf_rn(kk, s[j].z, pu.z);
-                pu.w = __fmaf_rn(kk, s[j].w, pu.w);
-                pw.x = __fmaf_rn(qq, s[j].x, pw.x);
-                pw.y = __fmaf_rn(qq, s[j].y, pw.y);
-                pw.z = __fmaf_rn(qq, s[j].z, pw.z);
-                pw.w = __fmaf_rn(qq, s[j].w, pw.w);
+                const float2 a2 = make_float2(a, a), k2 = make_float2(kk, kk), q2 = make_float2(qq, qq);
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    s[j][h2] = __fmul2_rn(s[j][h2], a2);             // decay
+                    pu[h2] = __ffma2_rn(k2, s[j][h2], pu[h2]);       // k . S'
+                    pw[h2] = __ffma2_rn(q2, s[j][h2], pw[h2]);       // q . S'
+                }
                 pqk = __fmaf_rn(qq, kk, pqk);
             }
             // sums over the 8 row groups (lane bits 2..4): a butterfly, after which every lane
             // holds the same bits (each level adds the same two values in either order)
 #pragma unroll
             for (int m = 4; m < 32; m <<= 1) {
-                pu.x = __fadd_rn(pu.x, __shfl_xor_sync(0xffffffffu, pu.x, m));
-                pu.y = __fadd_rn(pu.y, __shfl_xor_sync(0xffffffffu, pu.y, m));
-                pu.z = __fadd_rn(pu.z, __shfl_xor_sync(0xffffffffu, pu.z, m));
-                pu.w = __fadd_rn(pu.w, __shfl_xor_sync(0xffffffffu, pu.w, m));
-                pw.x = __fadd_rn(pw.x, __shfl_xor_sync(0xffffffffu, pw.x, m));
-                pw.y = __fadd_rn(pw.y, __shfl_xor_sync(0xffffffffu, pw.y, m));
-                pw.z = __fadd_rn(pw.z, __shfl_xor_sync(0xffffffffu, pw.z, m));
-                pw.w = __fadd_rn(pw.w, __shfl_xor_sync(0xffffffffu, pw.w, m));
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    pu[h2] = __fadd2_rn(pu[h2], make_float2(__shfl_xor_sync(0xffffffffu, pu[h2].x, m),
+                                                            __shfl_xor_sync(0xffffffffu, pu[h2].y, m)));
+                    pw[h2] = __fadd2_rn(pw[h2], make_float2(__shfl_xor_sync(0xffffffffu, pw[h2].x, m),
+                                                            __shfl_xor_sync(0xffffffffu, pw[h2].y, m)));
+                }
                 pqk = __fadd_rn(pqk, __shfl_xor_sync(0xffffffffu, pqk, m));
             }
-            const float4 u = pu, w = pw;
-            const float qk = pqk;
             const float bt = sb[tt];
             const float4 vv = *reinterpret_cast<const float4 *>(&sv[tt][cg * 4]);
-            float4 d;
-            d.x = __fmul_rn(bt, __fsub_rn(vv.x, u.x));
-            d.y = __fmul_rn(bt, __fsub_rn(vv.y, u.y));
-            d.z = __fmul_rn(bt, __fsub_rn(vv.z, u.z));
-            d.w = __fmul_rn(bt, __fsub_rn(vv.w, u.w));
+            // d = beta (v - u), per column
+            float2 d[2];
+            d[0] = make_float2(__fmul_rn(bt, __fsub_rn(vv.x, pu[0].x)), __fmul_rn(bt, __fsub_rn(vv.y, pu[0].y)));
+            d[1] = make_float2(__fmul_rn(bt, __fsub_rn(vv.z, pu[1].x)), __fmul_rn(bt, __fsub_rn(vv.w, pu[1].y)));
             // the state after a verify program's last token is never read (no commit, and o comes
             // from w, q.k and d): its update is skipped
             if (COMMIT_END || t != steps - 1) {
 #pragma unroll
                 for (int j = 0; j < RPT; ++j) {
                     const float kk = f4_at(k4[j >> 2], j & 3);
-                    s[j].x = __fmaf_rn(kk, d.x, s[j].x);
-                    s[j].y = __fmaf_rn(kk, d.y, s[j].y);
-                    s[j].z = __fmaf_rn(kk, d.z, s[j].z);
-                    s[j].w = __fmaf_rn(kk, d.w, s[j].w);
+                    const float2 k2 = make_float2(kk, kk);
+                    s[j][0] = __ffma2_rn(k2, d[0], s[j][0]);
+                    s[j][1] = __ffma2_rn(k2, d[1], s[j][1]);
                 }
             }
             if (WRITE_O && t >= n_pre && rg == 0) {
-                float4 o;
-                o.x = __fmaf_rn(qk, d.x, w.x);
-                o.y = __fmaf_rn(qk, d.y, w.y);
-                o.z = __fmaf_rn(qk, d.z, w.z);
-                o.w = __fmaf_rn(qk, d.w, w.w);
+                const float2 qk2 = make_float2(pqk, pqk);
+                const float2 o0 = __ffma2_rn(qk2, d[0], pw[0]), o1 = __ffma2_rn(qk2, d[1], pw[1]);
                 const size_t oo = token_row(t) * DV + col0 + cg * 4;
                 if (p.o_bf16) {
-                    uint2 pk = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+                    uint2 pk = make_uint2(pack_bf16x2(o0.x, o0.y), pack_bf16x2(o1.x, o1.y));
                     *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.o) + oo) = pk;
                 } else {
-                    *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + oo) = o;
+                    *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + oo) =
+                        make_float4(o0.x, o0.y, o1.x, o1.y);
                 }
             }
             if (MODE == kReplayVerify && t + 1 == n_pre) {
                 // the replayed prefix is the new committed state; the new window is only verified
-#pragma unroll
-                for (int j = 0; j < RPT; ++j)
-                    *reinterpret_cast<float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV) = s[j];
+                store_state();
             }
         }
     }
 
-    if (COMMIT_END) {
-#pragma unroll
-        for (int j = 0; j < RPT; ++j)
-            *reinterpret_cast<float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV) = s[j];
-    }
+    if (COMMIT_END) store_state();
 }
 
 template <int DK, int MODE>
 int launch_dk(int cw, const KdaParams &p, cudaStream_t st) {
     const int grid_per_head = DK / cw;
     const dim3 grid((unsigned)((size_t)p.B * p.H * grid_per_head));
+    cudaError_t e;
     trace_before(kTraceKda, st);
     switch (cw) {
-        case 16: kda_recur_kernel<DK, 16, MODE><<<grid, kRowGroups * 4, 0, st>>>(p); break;
-        case 32: kda_recur_kernel<DK, 32, MODE><<<grid, kRowGroups * 8, 0, st>>>(p); break;
-        case 64: kda_recur_kernel<DK, 64, MODE><<<grid, kRowGroups * 16, 0, st>>>(p); break;
+        case 16: e = launch_kernel(kda_recur_kernel<DK, 16, MODE>, grid, dim3(kRowGroups * 4), 0, st, p); break;
+        case 32: e = launch_kernel(kda_recur_kernel<DK, 32, MODE>, grid, dim3(kRowGroups * 8), 0, st, p); break;
+        case 64: e = launch_kernel(kda_recur_kernel<DK, 64, MODE>, grid, dim3(kRowGroups * 16), 0, st, p); break;
         case 128:
             if constexpr (DK >= 128 && MODE != kReplayVerify) {
-                kda_recur_kernel<DK, 128, MODE><<<grid, kRowGroups * 32, 0, st>>>(p);
+                e = launch_kernel(kda_recur_kernel<DK, 128, MODE>, grid, dim3(kRowGroups * 32), 0, st, p);
                 break;
             } else {
                 return HLA_ERR_UNSUPPORTED;
@@ -328,7 +338,7 @@ int launch_dk(int cw, const KdaParams &p, cudaStream_t st) {
         default: return HLA_ERR_UNSUPPORTED;
     }
     trace_after(kTraceKda, st);
-    return launch_status();
+    return launched(e);
 }
 
 // Column-slice width.  Measured on GB300 (d = 128, 32 heads, CUDA graphs, states rotated
@@ -421,6 +431,7 @@ int run_kda(int mode, int B, int T, int H, int dk, int dv, float *S, const int32
 __global__ void accept_prefix_kernel(int B, int T, const int32_t *__restrict__ draft,
                                      const int32_t *__restrict__ target, int32_t *accepted,
                                      int32_t *committed) {
+    pdl_wait_trigger();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     int n = 0;
@@ -453,6 +464,10 @@ extern "C" int kda_spec_verify_replay(int phase, int B, int T, int H, int dk, in
     if (phase == HLA_SPEC_REPLAY)
         return run_kda(kReplay, B, T, H, dk, dv, S, state_idx, q, k, v, alpha, beta,
                        accepted_len, nullptr, o_dtype, (cudaStream_t)stream);
+    // BOTH: a window's accepted length depends on what the target makes of that window's
+    // verify outputs, so its verify and its replay cannot share one call; the one-pass
+    // speculative step is kda_spec_replay_verify (previous window's replay + next verify)
+    if (phase == HLA_SPEC_BOTH) return HLA_ERR_UNSUPPORTED;
     return HLA_ERR_INVALID_ARG;
 }
 
@@ -487,7 +502,7 @@ extern "C" int spec_accept_prefix(int B, int T, const int32_t *draft_ids,
                     aligned16(committed_len),
                 HLA_ERR_MISALIGNED);
     set_variant("accept_prefix");
-    accept_prefix_kernel<<<(B + 127) / 128, 128, 0, (cudaStream_t)stream>>>(
-        B, T, draft_ids, target_ids, accepted_len, committed_len);
-    return launch_status();
+    return launched(launch_kernel(accept_prefix_kernel, dim3((B + 127) / 128), dim3(128), 0,
+                                  (cudaStream_t)stream, B, T, draft_ids, target_ids, accepted_len,
+                                  committed_len));
 }

@@ -210,6 +210,7 @@ __device__ int block_exclusive_scan(int v, int *warp_tot, int &total) {
 __global__ void __launch_bounds__(kDispatchThreads) moe_dispatch_kernel(const MoeArgs a) {
     __shared__ int cnt[1024], base[1024], run[1024], uid[1024];
     __shared__ int warp_tot[33];
+    pdl_wait_trigger();
     const int tid = threadIdx.x;
     const int npairs = a.M * a.k;
     const int nrb_gu = (a.I + 15) / 16, nrb_dn = (a.Hd + 31) / 32;
@@ -313,6 +314,7 @@ __device__ __forceinline__ int find_unit(const int *pref, int U, int it) {
 
 template <int NT, int UNROLL>
 __global__ void __launch_bounds__(kMoeThreads) moe_gateup_kernel(const MoeArgs a) {
+    pdl_wait_trigger();
     const int U = a.meta[0];
     const int total = a.item_gu[U];
     const int g = (threadIdx.x & 31) >> 2;
@@ -370,6 +372,7 @@ __global__ void __launch_bounds__(kMoeThreads) moe_gateup_kernel(const MoeArgs a
 }
 
 __global__ void moe_swiglu_reduce_kernel(const MoeArgs a) {
+    pdl_wait_trigger();
     const int n = a.meta[0];
     const int used = a.unit_off[n];  // positions in use
     // positions of shared experts on the tensor-core path are not grouped units: skip them
@@ -389,6 +392,7 @@ __global__ void moe_swiglu_reduce_kernel(const MoeArgs a) {
 
 template <int NT>
 __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(const MoeArgs a) {
+    pdl_wait_trigger();
     const int U = a.meta[0];
     const int total = a.item_dn[U];
     const int g = (threadIdx.x & 31) >> 2;
@@ -467,6 +471,7 @@ constexpr int xi_min_blocks(int NT, int UNROLL) { return (NT == 1 || UNROLL == 2
 template <int NT, int UNROLL>
 __global__ void __launch_bounds__(kMoeThreads, xi_min_blocks(NT, UNROLL))
     moe_gateup_xi_kernel(const MoeArgs a) {
+    pdl_wait_trigger();
     const int U = a.meta[0];
     const int total = a.item_gu[U];
     const int g = (threadIdx.x & 31) >> 2;
@@ -532,6 +537,7 @@ struct DownCtx {
 template <int NT, int UNROLL>
 __global__ void __launch_bounds__(kMoeThreads, xi_min_blocks(NT, UNROLL))
     moe_down_xi_kernel(const MoeArgs a) {
+    pdl_wait_trigger();
     const int U = a.meta[0];
     const int total = a.item_dn[U];
     const int g = (threadIdx.x & 31) >> 2;
@@ -593,6 +599,7 @@ __global__ void __launch_bounds__(kMoeThreads, xi_min_blocks(NT, UNROLL))
 // entries and all their slice rows loaded before any of them is used, so each group of four
 // slots costs one round of memory latency.
 __global__ void moe_combine_kernel(const MoeArgs a) {
+    pdl_wait_trigger();
     const int m = blockIdx.y;
     const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
     if (c4 * 4 >= a.Hd) return;
@@ -652,6 +659,7 @@ __global__ void moe_combine_kernel(const MoeArgs a) {
 // written into the shared expert's h rows (positions s*M .. s*M+M-1).
 __global__ void shared_swiglu_kernel(const float *__restrict__ pg, const float *__restrict__ pu,
                                      int split, int M, int I, uint16_t *h) {
+    pdl_wait_trigger();
     const size_t total = (size_t)M * I;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
@@ -667,6 +675,7 @@ __global__ void shared_swiglu_kernel(const float *__restrict__ pg, const float *
 // Sum of the down-projection slices into the (token, slot) rows of the expert outputs.
 __global__ void shared_down_reduce_kernel(const float *__restrict__ pd, int split, int M, int Hd,
                                           int S, int slot, float *ypart) {
+    pdl_wait_trigger();
     const size_t total = (size_t)M * Hd;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
@@ -712,45 +721,45 @@ int moe_ring_depth(bool gateup) {
 }
 
 template <int NT, int R, typename F>
-void launch_gateup_ring(F budgeted, const MoeArgs &a, cudaStream_t st) {
+cudaError_t launch_gateup_ring(F budgeted, const MoeArgs &a, cudaStream_t st) {
     static int g = 0;
     if (!g) g = persistent_grid(moe_gateup_xi_kernel<NT, R>);
-    moe_gateup_xi_kernel<NT, R><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+    return launch_kernel(moe_gateup_xi_kernel<NT, R>, dim3(budgeted(g)), dim3(kMoeThreads), 0, st, a);
 }
 
 template <int NT, int R, typename F>
-void launch_down_ring(F budgeted, const MoeArgs &a, cudaStream_t st) {
+cudaError_t launch_down_ring(F budgeted, const MoeArgs &a, cudaStream_t st) {
     static int g = 0;
     if (!g) g = persistent_grid(moe_down_xi_kernel<NT, R>);
-    moe_down_xi_kernel<NT, R><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+    return launch_kernel(moe_down_xi_kernel<NT, R>, dim3(budgeted(g)), dim3(kMoeThreads), 0, st, a);
 }
 
 template <typename F>
-void launch_gateup_xi(int TT, int ring, F budgeted, const MoeArgs &a, cudaStream_t st) {
+cudaError_t launch_gateup_xi(int TT, int ring, F budgeted, const MoeArgs &a, cudaStream_t st) {
     if (TT == 8) {
-        if (ring == 2) launch_gateup_ring<1, 2>(budgeted, a, st);
-        else if (ring == 3) launch_gateup_ring<1, 3>(budgeted, a, st);
-        else launch_gateup_ring<1, 4>(budgeted, a, st);
-    } else {
-        if (ring == 2) launch_gateup_ring<2, 2>(budgeted, a, st);
-        else if (ring == 3) launch_gateup_ring<2, 3>(budgeted, a, st);
-        else launch_gateup_ring<2, 4>(budgeted, a, st);
+        if (ring == 2) return launch_gateup_ring<1, 2>(budgeted, a, st);
+        if (ring == 3) return launch_gateup_ring<1, 3>(budgeted, a, st);
+        return launch_gateup_ring<1, 4>(budgeted, a, st);
     }
+    if (ring == 2) return launch_gateup_ring<2, 2>(budgeted, a, st);
+    if (ring == 3) return launch_gateup_ring<2, 3>(budgeted, a, st);
+    return launch_gateup_ring<2, 4>(budgeted, a, st);
 }
 
 template <typename F>
-void launch_down_xi(int TT, int ring, F budgeted, const MoeArgs &a, cudaStream_t st) {
+cudaError_t launch_down_xi(int TT, int ring, F budgeted, const MoeArgs &a, cudaStream_t st) {
     if (TT == 8) {
-        if (ring == 2) launch_down_ring<1, 2>(budgeted, a, st);
-        else if (ring == 3) launch_down_ring<1, 3>(budgeted, a, st);
-        else launch_down_ring<1, 4>(budgeted, a, st);
-    } else {
-        if (ring == 2) launch_down_ring<2, 2>(budgeted, a, st);
-        else if (ring == 3) launch_down_ring<2, 3>(budgeted, a, st);
-        else launch_down_ring<2, 4>(budgeted, a, st);
+        if (ring == 2) return launch_down_ring<1, 2>(budgeted, a, st);
+        if (ring == 3) return launch_down_ring<1, 3>(budgeted, a, st);
+        return launch_down_ring<1, 4>(budgeted, a, st);
     }
+    if (ring == 2) return launch_down_ring<2, 2>(budgeted, a, st);
+    if (ring == 3) return launch_down_ring<2, 3>(budgeted, a, st);
+    return launch_down_ring<2, 4>(budgeted, a, st);
 }
 
+// Fork/join events of a side stream, per host thread and per device (an event belongs to the
+// device that was current when it was created).
 struct SideStreamEvents {
     cudaEvent_t fork = nullptr, join = nullptr;
     bool ok() {
@@ -759,7 +768,16 @@ struct SideStreamEvents {
         return true;
     }
 };
-thread_local SideStreamEvents g_moe_events;
+constexpr int kMaxDevices = 64;
+// role 0: the shared experts' L2 prefetch; role 1: the shared experts on the side stream
+thread_local SideStreamEvents g_side_events[2][kMaxDevices];
+
+SideStreamEvents *side_events(int role) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    SideStreamEvents *e = &g_side_events[role][dev];
+    return e->ok() ? e : nullptr;
+}
 
 
 // The shared experts as dense SwiGLUs over all M tokens: gate and up products (split K,
@@ -787,16 +805,17 @@ int run_shared_dense(const MoeLayout &L, bool tc, const hla_bf16 *x, const hla_b
         hla_bf16 *hs = h + (size_t)s * M * I;
         if ((r = proj(I, Hd, x, Ws_gate + eo, sgu, pg)) != HLA_OK) return r;
         if ((r = proj(I, Hd, x, Ws_up + eo, sgu, pu)) != HLA_OK) return r;
-        shared_swiglu_kernel<<<grid, 256, 0, st>>>(pg, pu, sgu, M, I, hs);
-        if ((r = launch_status()) != HLA_OK) return r;
+        if ((r = launched(launch_kernel(shared_swiglu_kernel, dim3(grid), dim3(256), 0, st, (const float *)pg,
+                                        (const float *)pu, sgu, M, I, reinterpret_cast<uint16_t *>(hs)))) != HLA_OK)
+            return r;
         if ((r = proj(Hd, I, hs, Ws_down + eo, sdn, pd)) != HLA_OK) return r;
-        shared_down_reduce_kernel<<<grid, 256, 0, st>>>(pd, sdn, M, Hd, L.k + L.nsh, L.k + s, ypart);
-        if ((r = launch_status()) != HLA_OK) return r;
+        if ((r = launched(launch_kernel(shared_down_reduce_kernel, dim3(grid), dim3(256), 0, st, (const float *)pd,
+                                        sdn, M, Hd, L.k + L.nsh, L.k + s, ypart))) != HLA_OK)
+            return r;
     }
     return HLA_OK;
 }
 
-thread_local SideStreamEvents g_shared_events;
 
 }  // namespace
 
@@ -827,13 +846,14 @@ int moe_shared_side(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 
                     const hla_bf16 *Ws_gate, const hla_bf16 *Ws_up, const hla_bf16 *Ws_down,
                     void *ws, cudaStream_t st, cudaStream_t side) {
     const MoeLayout L = moe_layout(M, Hd, I, E, k, nsh);
-    if (!g_shared_events.ok()) return HLA_ERR_CUDA;
-    if (cudaEventRecord(g_shared_events.fork, st) != cudaSuccess) return HLA_ERR_CUDA;
-    if (cudaStreamWaitEvent(side, g_shared_events.fork, 0) != cudaSuccess) return HLA_ERR_CUDA;
+    SideStreamEvents *ev = side_events(1);
+    if (!ev) return HLA_ERR_CUDA;
+    if (cudaEventRecord(ev->fork, st) != cudaSuccess) return HLA_ERR_CUDA;
+    if (cudaStreamWaitEvent(side, ev->fork, 0) != cudaSuccess) return HLA_ERR_CUDA;
     const int r = run_shared_dense(L, false, x, Ws_gate, Ws_up, Ws_down, reinterpret_cast<char *>(ws),
                                    side);
     if (r != HLA_OK) return r;
-    if (cudaEventRecord(g_shared_events.join, side) != cudaSuccess) return HLA_ERR_CUDA;
+    if (cudaEventRecord(ev->join, side) != cudaSuccess) return HLA_ERR_CUDA;
     return HLA_OK;
 }
 
@@ -873,10 +893,11 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     const int mask = pm >= 0 ? pm & (kPrefetchSharedGateUp | kPrefetchSharedDown)
                              : ((a.nsh_units > 0 && M > L.TT) ? kPrefetchSharedGateUp : 0);
     const bool side = pf != nullptr && nsh > 0 && mask != 0 && !shared_side;
+    SideStreamEvents *pev = side ? side_events(0) : nullptr;
     if (side) {
-        if (!g_moe_events.ok()) return HLA_ERR_CUDA;
-        if (cudaEventRecord(g_moe_events.fork, st) != cudaSuccess) return HLA_ERR_CUDA;
-        if (cudaStreamWaitEvent(pf, g_moe_events.fork, 0) != cudaSuccess) return HLA_ERR_CUDA;
+        if (!pev) return HLA_ERR_CUDA;
+        if (cudaEventRecord(pev->fork, st) != cudaSuccess) return HLA_ERR_CUDA;
+        if (cudaStreamWaitEvent(pf, pev->fork, 0) != cudaSuccess) return HLA_ERR_CUDA;
         const size_t mat = (size_t)nsh * I * Hd * sizeof(uint16_t);
         int r = HLA_OK;
         if (mask & kPrefetchSharedGateUp) {
@@ -885,7 +906,7 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
         }
         if (r == HLA_OK && (mask & kPrefetchSharedDown)) r = run_l2_prefetch(Ws_down, mat, pf);
         if (r != HLA_OK) return r;
-        if (cudaEventRecord(g_moe_events.join, pf) != cudaSuccess) return HLA_ERR_CUDA;
+        if (cudaEventRecord(pev->join, pf) != cudaSuccess) return HLA_ERR_CUDA;
     }
 
     int r;
@@ -905,52 +926,56 @@ int run_moe(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x, cons
     const bool xgu = moe_cross_item() && min_slice_steps(Hd, L.KS) >= ring_gu;
     const bool xdn = moe_cross_item() && min_slice_steps(I, L.KSD) >= ring_dn;
     const int dthreads = (int)round_up((size_t)(E + nsh), 32);
-    moe_dispatch_kernel<<<1, dthreads, 0, st>>>(a);
-    r = launch_status();
+    r = launched(launch_kernel(moe_dispatch_kernel, dim3(1), dim3(dthreads), 0, st, a));
     if (r != HLA_OK) return r;
     const int keep = shared_side ? sm_count() - shared_sm_budget() : sm_count();
     auto budgeted = [&](int full) { return full / sm_count() * keep; };
+    cudaError_t e;
+    const dim3 mt(kMoeThreads);
     trace_before(kTraceMoeGateup, st);
     if (xgu) {
-        launch_gateup_xi(L.TT, ring_gu, budgeted, a, st);
+        e = launch_gateup_xi(L.TT, ring_gu, budgeted, a, st);
     } else if (L.TT == 8) {
         static int g = 0;
         if (!g) g = persistent_grid(moe_gateup_kernel<1, 4>);
-        moe_gateup_kernel<1, 4><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+        e = launch_kernel(moe_gateup_kernel<1, 4>, dim3(budgeted(g)), mt, 0, st, a);
     } else if (shallow) {
         static int g = 0;
         if (!g) g = persistent_grid(moe_gateup_kernel<2, 2>);
-        moe_gateup_kernel<2, 2><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+        e = launch_kernel(moe_gateup_kernel<2, 2>, dim3(budgeted(g)), mt, 0, st, a);
     } else {
         static int g = 0;
         if (!g) g = persistent_grid(moe_gateup_kernel<2, 4>);
-        moe_gateup_kernel<2, 4><<<budgeted(g), kMoeThreads, 0, st>>>(a);
+        e = launch_kernel(moe_gateup_kernel<2, 4>, dim3(budgeted(g)), mt, 0, st, a);
     }
     trace_after(kTraceMoeGateup, st);
-    if ((r = launch_status()) != HLA_OK) return r;
+    if ((r = launched(e)) != HLA_OK) return r;
     if (L.KS > 1) {
-        moe_swiglu_reduce_kernel<<<4 * sm_count(), 256, 0, st>>>(a);
-        if ((r = launch_status()) != HLA_OK) return r;
+        if ((r = launched(launch_kernel(moe_swiglu_reduce_kernel, dim3(4 * sm_count()), dim3(256), 0, st, a))) !=
+            HLA_OK)
+            return r;
     }
     trace_before(kTraceMoeDown, st);
     if (xdn) {
-        launch_down_xi(L.TT, ring_dn, budgeted, a, st);
+        e = launch_down_xi(L.TT, ring_dn, budgeted, a, st);
     } else if (L.TT == 8) {
         static int d = 0;
         if (!d) d = persistent_grid(moe_down_kernel<1>);
-        moe_down_kernel<1><<<budgeted(d), kMoeThreads, 0, st>>>(a);
+        e = launch_kernel(moe_down_kernel<1>, dim3(budgeted(d)), mt, 0, st, a);
     } else {
         static int d = 0;
         if (!d) d = persistent_grid(moe_down_kernel<2>);
-        moe_down_kernel<2><<<budgeted(d), kMoeThreads, 0, st>>>(a);
+        e = launch_kernel(moe_down_kernel<2>, dim3(budgeted(d)), mt, 0, st, a);
     }
     trace_after(kTraceMoeDown, st);
-    if ((r = launch_status()) != HLA_OK) return r;
-    if (shared_side && cudaStreamWaitEvent(st, g_shared_events.join, 0) != cudaSuccess) return HLA_ERR_CUDA;
+    if ((r = launched(e)) != HLA_OK) return r;
+    if (shared_side) {
+        SideStreamEvents *sev = side_events(1);
+        if (!sev || cudaStreamWaitEvent(st, sev->join, 0) != cudaSuccess) return HLA_ERR_CUDA;
+    }
     const dim3 cgrid((unsigned)((Hd / 4 + 127) / 128), (unsigned)M);
-    moe_combine_kernel<<<cgrid, 128, 0, st>>>(a);
-    if ((r = launch_status()) != HLA_OK) return r;
-    if (side && cudaStreamWaitEvent(st, g_moe_events.join, 0) != cudaSuccess) return HLA_ERR_CUDA;
+    if ((r = launched(launch_kernel(moe_combine_kernel, cgrid, dim3(128), 0, st, a))) != HLA_OK) return r;
+    if (side && cudaStreamWaitEvent(st, pev->join, 0) != cudaSuccess) return HLA_ERR_CUDA;
     // kernel forms: ",xgu<ring>" / ",xdn<ring>" cross-item, ",u2" the shallow per-item gate/up
     char ringv[32] = "";
     int o = 0;

@@ -8,8 +8,6 @@
 // partials in a file-scope device array instead of a caller workspace.  The array is part
 // of the library's device image, so every GPU that loads the library holds it until the
 // process exits.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace hla {
@@ -19,6 +17,8 @@ int run_dense(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W, int spl
 int run_splitk_reduce(const float *part, int split, int M, int N, const hla_bf16 *residual, void *y,
                       int y_bf16, cudaStream_t st);
 int dense_tokens_per_tile(int M);
+bool dense_tc_enabled(int M);
+bool dense_xi_applies(int N, int K, int split);
 
 namespace {
 
@@ -26,24 +26,15 @@ namespace {
 constexpr size_t kScratchFloats = HLA_NOALLOC_SCRATCH_BYTES / sizeof(float);
 __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-float *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once per device
-// (the host-side name of a __device__ array is not a device address).
+// Device address of the scratch array on the current device.  The host-side name of a
+// __device__ array is not a device address, so it is asked for with the device current.
+// The answer is not cached: the query is a host-side table lookup, and a cached address
+// would dangle after a device reset reloads the library's device image elsewhere.  On the
+// first call on a device the runtime may load that image there.
 int scratch_for_current_device(float **out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return HLA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return HLA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-            return HLA_ERR_CUDA;
-        g_scratch_ptr[dev] = static_cast<float *>(p);
-    }
-    *out = g_scratch_ptr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return HLA_ERR_CUDA;
+    *out = static_cast<float *>(p);
     return HLA_OK;
 }
 
@@ -66,7 +57,9 @@ extern "C" int skinny_proj_splitk_noalloc(int M, int N, int K, const hla_bf16 *x
     HLA_REQUIRE(need <= kScratchFloats * sizeof(float), HLA_ERR_WORKSPACE);
     const int s = need == 0 ? 1 : (int)(need / ((size_t)M * N * sizeof(float)));
     cudaStream_t st = (cudaStream_t)stream;
-    set_variant("skinny_proj_noalloc<tt%d,split%d>", dense_tokens_per_tile(M), s);
+    // same variant text as skinny_proj_splitk after the prefix (which streaming kernel, which split)
+    set_variant("skinny_proj_noalloc<tt%d,%ssplit%d>", dense_tokens_per_tile(M),
+                !dense_tc_enabled(M) && dense_xi_applies(N, K, s) ? "xi," : "", s);
     if (s == 1) return run_dense(M, N, K, x, W, 1, nullptr, y, y_dtype == HLA_BF16, residual, st);
     float *scratch = nullptr;
     int r = scratch_for_current_device(&scratch);

@@ -42,12 +42,19 @@ __device__ __forceinline__ void mma_step(const uint4 (&wa)[NMAT][2], const uint4
 // K in [kb, ke) (multiples of 32).  wg[m] / wg8[m] point at weight rows g and g+8 of
 // matrix m (element 0 of the row); xr[nt] points at the token row that lane group g
 // feeds to tile nt.  Lanes whose rows / tokens fall outside the problem point at any
-// valid row; their outputs are simply not stored.
-template <int NMAT, int NT, int UNROLL>
+// valid row; their outputs are simply not stored.  before_x() runs between the weight loads
+// and the token loads of the first UNROLL steps (the place for a programmatic-launch wait: the
+// weights are static, the tokens come from the preceding kernel).
+struct NoHook {
+    __device__ __forceinline__ void operator()() const {}
+};
+
+template <int NMAT, int NT, int UNROLL, class Hook = NoHook>
 __device__ __forceinline__ void warp_stream_tile(const uint16_t *const (&wg)[NMAT],
                                                  const uint16_t *const (&wg8)[NMAT],
                                                  const uint16_t *const (&xr)[NT], int kb, int ke,
-                                                 float (&acc)[NMAT][NT][4]) {
+                                                 float (&acc)[NMAT][NT][4],
+                                                 const Hook &before_x = Hook()) {
     const int t8 = (threadIdx.x & 3) * 8;
     const int nsteps = (ke - kb) >> 5;
     uint4 wa[UNROLL][NMAT][2];
@@ -62,6 +69,13 @@ __device__ __forceinline__ void warp_stream_tile(const uint16_t *const (&wg)[NMA
                 wa[u][m][0] = ld_weight_v4(wg[m] + k);
                 wa[u][m][1] = ld_weight_v4(wg8[m] + k);
             }
+        }
+    }
+    before_x();
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+        if (u < nsteps) {
+            const int k = kb + 32 * u + t8;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) xb[u][nt] = ld_act_v4(xr[nt] + k);
         }
@@ -136,16 +150,23 @@ struct ItemRows {
     const uint16_t *x[NT];
     int n;
     Ctx ctx;
-    __device__ __forceinline__ void load(int s, size_t ld8, uint4 (&wa)[NMAT][2],
-                                         uint4 (&xb)[NT]) const {
+    __device__ __forceinline__ void load_w(int s, size_t ld8, uint4 (&wa)[NMAT][2]) const {
         const int k = 32 * s + (threadIdx.x & 3) * 8;
 #pragma unroll
         for (int m = 0; m < NMAT; ++m) {
             wa[m][0] = ld_weight_v4(w[m] + k);
             wa[m][1] = ld_weight_v4(w[m] + ld8 + k);
         }
+    }
+    __device__ __forceinline__ void load_x(int s, uint4 (&xb)[NT]) const {
+        const int k = 32 * s + (threadIdx.x & 3) * 8;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) xb[nt] = ld_act_v4(x[nt] + k);
+    }
+    __device__ __forceinline__ void load(int s, size_t ld8, uint4 (&wa)[NMAT][2],
+                                         uint4 (&xb)[NT]) const {
+        load_w(s, ld8, wa);
+        load_x(s, xb);
     }
 };
 
@@ -169,10 +190,13 @@ struct StridedClaims {
 
 // claims: first() -> the warp's first item, issue() at the claim point, take() -> the next
 // item (>= total: none).  decode(it) -> ItemRows of item it; epilogue(ctx, acc) stores an
-// item's result.
-template <int NMAT, int NT, int UNROLL, class Ctx, class Claims, class Decode, class Epilogue>
+// item's result.  before_x() runs between the weight loads and the token loads of the first
+// ring (as in warp_stream_tile).
+template <int NMAT, int NT, int UNROLL, class Ctx, class Claims, class Decode, class Epilogue,
+          class Hook = NoHook>
 __device__ __forceinline__ void stream_items(Claims &claims, int total, size_t ld8,
-                                             const Decode &decode, const Epilogue &epilogue) {
+                                             const Decode &decode, const Epilogue &epilogue,
+                                             const Hook &before_x = Hook()) {
     using Item = ItemRows<NMAT, NT, Ctx>;
     int it = claims.first();
     if (it >= total) return;
@@ -184,7 +208,10 @@ __device__ __forceinline__ void stream_items(Claims &claims, int total, size_t l
     float acc[NMAT][NT][4];
     zero_acc<NMAT, NT>(acc);
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) cur.load(u, ld8, wa[u], xb[u]);
+    for (int u = 0; u < UNROLL; ++u) cur.load_w(u, ld8, wa[u]);
+    before_x();
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) cur.load_x(u, xb[u]);
     int ls = 0;  // the step of cur that ring slot u holds
     for (;;) {
 #pragma unroll

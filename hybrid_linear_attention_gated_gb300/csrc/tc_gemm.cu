@@ -13,10 +13,25 @@
 //   * all four warps then read the accumulator back with tcgen05.ld (warp w owns TMEM lanes
 //     32w..32w+31 = weight rows) and store fp32 partials or the final output.
 // Each weight byte is read from HBM once and multiplied against all MT tokens from
-// shared memory.  Every wait is bounded: a wait that gives up records
+// shared memory.  Every wait is bounded in time: a wait that gives up records
 // HLA_ERR_DEVICE_TIMEOUT in a device status word and the CTA drains and exits.
+//
+// Drain order (so that a CTA never touches tensor memory that its own MMAs may still write,
+// and never exits holding tensor memory or with copies landing in its shared memory):
+//   1. the MMA thread issues an MMA only after the stage's TMA fill has completed, so every
+//      issued MMA reads operands already in shared memory;
+//   2. after its loop (complete or given up) it commits `done`, which completes once every
+//      MMA it issued has finished, and waits for that itself;
+//   3. a block barrier publishes the outcome; tensor memory is read only if `done` completed;
+//   4. the producer waits for every fill it issued that no MMA consumed;
+//   5. tensor memory is freed after `done` has completed.  A `done` that does not complete
+//      within the limit is waited for again with a longer one.  That cannot happen for MMAs
+//      whose operands were already resident.  If it does anyway, the memory is freed all the
+//      same, because a CTA that exits holding tensor memory blocks every later allocation on
+//      its SM; the status word has already flagged the launch.
 #include <cuda.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -31,9 +46,19 @@ namespace {
 constexpr int kTcThreads = 128;
 constexpr int kRows = 128;    // MMA M: weight rows per CTA
 constexpr int kChunk = 64;    // K elements per stage = one 128-byte swizzle atom of bf16
-constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s of %globaltimer per bounded wait
 
 __device__ int g_tc_status = 0;
+// Test hook (hla_test_force_wait_timeout): while set, the launches carry force_timeout = 1,
+// and CTA 0 of each makes one bounded wait give up on a barrier that nothing arrives at; every
+// CTA then returns before it allocates tensor memory or issues a copy or an MMA.
+std::atomic<int> g_force_timeout{0};
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -49,10 +74,13 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
-// Bounded wait for the phase with the given parity; false (and the status word set) on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Wait for the phase with the given parity for at most limit_ns of %globaltimer; false (and
+// the status word set) if it has not completed by then.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_u32(bar);
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
         uint32_t done;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -61,6 +89,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
             : "r"(a), "r"(parity)
             : "memory");
         if (done) return true;
+        if ((i & 63) == 0) {  // the clock is read every 64 polls
+            const uint64_t t = global_ns();
+            if (i == 0) t0 = t;
+            else if (t - t0 > limit_ns) break;
+        }
     }
     atomicExch(&g_tc_status, HLA_ERR_DEVICE_TIMEOUT);
     return false;
@@ -134,6 +167,7 @@ struct TcParams {
     void *y;
     int y_bf16;
     const uint16_t *residual;
+    int force_timeout;         // test hook, see g_force_timeout
 };
 
 template <int MT>
@@ -144,7 +178,7 @@ __host__ __device__ constexpr int tc_stages() {
 template <int MT>
 __host__ __device__ constexpr size_t tc_smem_bytes() {
     return 1024 + static_cast<size_t>(tc_stages<MT>()) * (kRows * 128 + MT * 128) +
-           (2 * tc_stages<MT>() + 1) * 8 + 16;  // + TMEM address and consumed count
+           (2 * tc_stages<MT>() + 1) * 8 + 16;  // + TMEM address, consumed count, drained flag
 }
 
 template <int MT>
@@ -163,6 +197,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *done = empty + NS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     int *consumed_slot = reinterpret_cast<int *>(tmem_slot + 1);
+    int *drained_slot = consumed_slot + 1;
+
+    if (p.force_timeout) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            mbar_init(done, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            mbar_wait(done, 0, 1000000ull);  // nothing arrives: gives up after 1 ms
+            asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(done)) : "memory");
+        }
+        return;
+    }
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rb = blockIdx.x % p.nrb, ks = blockIdx.x / p.nrb;
@@ -190,11 +235,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x != 0) pdl_wait_trigger();  // the producer waits after its first weight copies
 
     int issued = 0, consumed = 0;
     if (warp == 0 && lane == 0) {
-        // producer: TMA the weight tile and the token tile of each K chunk
-        for (int i = 0; i < nmine; ++i) {
+        // producer: TMA the weight tile and the token tile of each K chunk.  The weights are
+        // static, so the first ring's weight tiles go out before waiting for the kernel that
+        // writes the tokens (a programmatic launch; otherwise the wait returns at once).
+        const int pre = nmine < NS ? nmine : NS;
+        for (int i = 0; i < pre; ++i) {
+            mbar_expect_tx(&full[i], A_BYTES + B_BYTES);
+            tma_load_2d(sA + i * A_BYTES, &tmW, (c0 + i) * kChunk, rb * kRows, &full[i]);
+        }
+        pdl_wait_trigger();
+        for (int i = 0; i < pre; ++i) {
+            tma_load_2d(sB + i * B_BYTES, &tmX, (c0 + i) * kChunk, 0, &full[i]);
+            issued = i + 1;
+        }
+        for (int i = pre; i < nmine; ++i) {
             const int s = i % NS;
             if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1)) break;
             mbar_expect_tx(&full[s], A_BYTES + B_BYTES);
@@ -218,18 +276,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             consumed = i + 1;
         }
         umma_commit(done);  // arrives once every MMA issued above has completed
+        // the MMAs read operands already in shared memory, so `done` completes; a second,
+        // longer wait covers the case that it has not within the first limit
+        const bool drained = mbar_wait(done, 0) || mbar_wait(done, 0, 8 * kWaitLimitNs);
         *consumed_slot = consumed;
+        *drained_slot = drained ? 1 : 0;
     }
     __syncwarp();
-
-    const bool ok = mbar_wait(done, 0);
+    __syncthreads();  // publishes consumed_slot / drained_slot
     tc_fence_after();
+    const bool drained = *drained_slot != 0;
     const int row = rb * kRows + warp * 32 + lane;
-    const bool have = ok && nmine > 0;
+    // every chunk multiplied and every MMA finished: the accumulator is the result
+    const bool have = drained && *consumed_slot == nmine && nmine > 0;
 #pragma unroll
     for (int c = 0; c < MT; c += 16) {
         uint32_t v[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+        if (drained) tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
         if (row < p.N) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -250,12 +313,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
     }
-    // after a timeout, copies may be in flight that no MMA waited for: wait (bounded) for
-    // those fills before the CTA exits.  At most one unconsumed fill per stage exists, since
-    // the producer never runs more than NS fills ahead of the MMA thread.
-    __syncthreads();
+    // after a timeout, copies may be in flight that no MMA waited for: wait for those fills
+    // before the CTA exits (each bounded, then once more with a longer limit).  At most one
+    // unconsumed fill per stage exists, since the producer never runs more than NS fills
+    // ahead of the MMA thread.
     if (warp == 0 && lane == 0) {
-        for (int i = *consumed_slot; i < issued; ++i) mbar_wait(&full[i % NS], (i / NS) & 1);
+        for (int i = *consumed_slot; i < issued; ++i)
+            if (!mbar_wait(&full[i % NS], (i / NS) & 1)) mbar_wait(&full[i % NS], (i / NS) & 1, 8 * kWaitLimitNs);
     }
     tc_fence_before();
     __syncthreads();
@@ -311,9 +375,10 @@ int launch_tc(const TcParams &p, const void *W, const void *x, cudaStream_t st) 
     CUtensorMap mw, mx;
     if (!make_map(&mw, W, p.N, p.K, kRows) || !make_map(&mx, x, p.M, p.K, MT)) return HLA_ERR_CUDA;
     trace_before(kTraceDense, st);
-    dense_tc_kernel<MT><<<p.nrb * p.split, kTcThreads, tc_smem_bytes<MT>(), st>>>(mw, mx, p);
+    const cudaError_t e = launch_kernel(dense_tc_kernel<MT>, dim3(p.nrb * p.split), dim3(kTcThreads),
+                                        tc_smem_bytes<MT>(), st, mw, mx, p);
     trace_after(kTraceDense, st);
-    return launch_status();
+    return launched(e);
 }
 
 }  // namespace
@@ -365,6 +430,7 @@ int run_dense_tc(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W, int 
     p.split = split;
     p.chunks_per_split = (p.nchunks + split - 1) / split;
     p.part = part; p.y = y; p.y_bf16 = y_bf16; p.residual = residual;
+    p.force_timeout = g_force_timeout.load(std::memory_order_relaxed);
     switch (dense_tc_tile(M)) {
         case 32: return launch_tc<32>(p, W, x, st);
         case 64: return launch_tc<64>(p, W, x, st);
@@ -374,6 +440,13 @@ int run_dense_tc(int M, int N, int K, const hla_bf16 *x, const hla_bf16 *W, int 
 }
 
 }  // namespace hla
+
+// Test hook: while on != 0, every tensor-core launch records HLA_ERR_DEVICE_TIMEOUT through one
+// bounded wait that gives up, and writes no output; nothing is allocated, copied or multiplied.
+extern "C" int hla_test_force_wait_timeout(int on) {
+    hla::g_force_timeout.store(on ? 1 : 0, std::memory_order_relaxed);
+    return HLA_OK;
+}
 
 // Reads and clears the status word the tensor-core kernels set when a bounded wait gives up.
 extern "C" int hla_device_status(void) {

@@ -18,6 +18,7 @@ HLA_F32 = 0
 HLA_BF16 = 1
 HLA_SPEC_VERIFY = 1
 HLA_SPEC_REPLAY = 2
+HLA_SPEC_BOTH = 3  # named by the ABI, answered with HLA_ERR_UNSUPPORTED (see include/hla.h)
 
 _lib = None
 
@@ -70,6 +71,7 @@ SIGNATURES = {
     "skinny_proj_splitk_noalloc": (c_int, [c_int] * 3 + [P] * 4 + [c_int, c_int, P]),
     "hla_launch_count": (ctypes.c_ulonglong, []),
     "hla_device_status": (c_int, []),
+    "hla_test_force_wait_timeout": (c_int, [c_int]),
     "hla_trace_enable": (c_int, [c_char_p, c_int]),
     "hla_trace_read": (c_int, [ctypes.POINTER(c_float), c_int]),
 }
@@ -292,3 +294,7 @@ def skinny_proj_splitk_noalloc(M, N, K, x, W, residual, y, y_dtype, split, strea
 
 def hla_device_status():
     return load().hla_device_status()
+
+
+def hla_test_force_wait_timeout(on):
+    return _check("hla_test_force_wait_timeout", load().hla_test_force_wait_timeout(int(on)))

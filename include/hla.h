@@ -37,8 +37,20 @@
  *  - Arguments are validated on the host before any launch; invalid ones return
  *    HLA_ERR_INVALID_ARG / HLA_ERR_UNSUPPORTED and leave all buffers untouched.
  *  - A failed launch returns HLA_ERR_CUDA (cudaGetLastError is consumed).
- *  - Entry points are stateless and reentrant; calls on different streams may
- *    run concurrently when their buffers do not overlap.
+ *  - Entry points keep no state between calls apart from: the device status word
+ *    (hla_device_status), the calling thread's last-variant string, the
+ *    instrumentation counters, per-device cached attributes and per-thread events
+ *    of the side-stream fork/join, and the one scratch array shared by every
+ *    skinny_proj_splitk_noalloc call.  Calls on different streams may run
+ *    concurrently when their buffers do not overlap (skinny_proj_splitk_noalloc
+ *    excepted: see there).
+ *  - Projections of 32 or more tokens run on the tensor-core path, whose
+ *    pipeline waits are bounded: a wait that gives up does not fail the launch
+ *    but sets the device status word.  Every entry point that can reach that path
+ *    (skinny_proj_splitk, skinny_proj_splitk_noalloc, skinny_proj_residual_rmsnorm,
+ *    kda_qkvg_proj, moe_route_topk, moe_expert_forward, hla_decode_layer) can
+ *    therefore return HLA_OK with invalid outputs; a caller that must know checks
+ *    hla_device_status() after synchronising.
  *  - Results are deterministic: every reduction runs in a fixed order, so the
  *    same inputs give bit-identical outputs run to run.
  */
@@ -67,7 +79,7 @@ enum hla_status {
 
 enum hla_dtype { HLA_F32 = 0, HLA_BF16 = 1 };
 
-enum hla_spec_phase { HLA_SPEC_VERIFY = 1, HLA_SPEC_REPLAY = 2 };
+enum hla_spec_phase { HLA_SPEC_VERIFY = 1, HLA_SPEC_REPLAY = 2, HLA_SPEC_BOTH = 3 };
 
 /* Human-readable text for a status value (static storage). */
 const char *hla_status_string(int status);
@@ -117,6 +129,12 @@ int kda_decode_step(int B, int H, int dk, int dv, float *S, const int32_t *state
  *          first a tokens in order to S[slot(b), h] and store the result; for
  *          a = 0 the state is not touched at all.  o is ignored (may be NULL).
  *          accepted_len values are clamped to [0, T].
+ *  phase = HLA_SPEC_BOTH returns HLA_ERR_UNSUPPORTED and launches nothing.  The
+ *          accepted length of a window comes from the target's tokens, which the
+ *          target model computes from the verify outputs of that same window, so
+ *          a window's verify and its replay cannot share one call.  The one-pass
+ *          form of a speculative step is kda_spec_replay_verify: the replay of the
+ *          previous window's accepted prefix fused with the verify of the next.
  *  1 <= T <= 8; q, k [B, T, H, dk] bf16; v [B, T, H, dv] bf16;
  *  alpha [B, T, H, dk] fp32; beta [B, T, H] fp32; accepted_len int32 [B];
  *  o [B, T, H, dv] (o_dtype).  Other arguments as kda_decode_step.
@@ -345,8 +363,12 @@ int hla_decode_layer_routing(const hla_layer *L, int M, const void *ws, const in
  *  - The split is the one skinny_proj_splitk would use; when its partials
  *    (split x M x N x 4 bytes) do not fit the array the call returns HLA_ERR_WORKSPACE
  *    and launches nothing (pass a smaller split, e.g. 1, which needs no scratch).
- *  - The first call on each device looks up the array's device address (once per
- *    device, with that device current); make that first call before any stream capture.
+ *  - Every call asks the runtime for the array's device address on the current device
+ *    (a host-side lookup, so a device reset cannot leave a stale address behind).  The
+ *    first call on a device may also load the library's device code there; make that
+ *    first call before any stream capture.
+ *  - At 32 or more tokens it runs on the tensor-core path: check hla_device_status()
+ *    as the conventions above say.
  *  - All calls share the one array, so calls that can overlap on the GPU (different
  *    streams, or different host threads) race and give wrong results: serialise them.
  *    The array keeps the last call's partials; each call overwrites every partial it
@@ -373,6 +395,14 @@ unsigned long long hla_launch_count(void);
  * device-side wait (the tensor-core projection's pipeline barriers) gave up since the last
  * read.  Synchronous (copies 4 bytes from the device); HLA_ERR_CUDA if that copy fails. */
 int hla_device_status(void);
+/* Test hook for the failure path, with no counterpart on the source pages.  While on != 0,
+ * every tensor-core projection launch makes one of its bounded device waits give up (block 0
+ * waits 1 ms on a barrier that nothing arrives at) and records HLA_ERR_DEVICE_TIMEOUT, and
+ * every block returns before it allocates tensor memory or issues a copy or an MMA; the
+ * launch writes no output.  This lets a test check the status path without a real stall.
+ * Takes effect for launches made after the call (a CUDA graph keeps what it captured);
+ * process-wide, not thread-safe with concurrent launches.  Always returns HLA_OK. */
+int hla_test_force_wait_timeout(int on);
 int hla_trace_enable(const char *kernel, int capacity);
 int hla_trace_read(float *ms_out, int max_n);
 

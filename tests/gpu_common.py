@@ -1,5 +1,6 @@
 """Helpers shared by the GPU parity tests (comparison metrics, oracle-built warm states)."""
 
+import collections
 import functools
 
 import numpy as np
@@ -65,16 +66,31 @@ def warm_states(seed, B, H, d, P=64):
 FULL = dict(Hd=7168, I=2048, E=256, k=8, n_shared=1)
 
 
-class ExpertCache:
-    """Copies an expert's three matrices to the host in fp64 the first time the oracle asks."""
+def f64_big(t):
+    """Exact fp64 host copy of a large device tensor (widened on the device, then copied)."""
+    return t.detach().to(torch.float64).to("cpu").numpy()
 
-    def __init__(self, w):
-        self.w, self.cache = w, {}
+
+class ExpertCache:
+    """An expert's three matrices as fp64 host arrays, fetched when the oracle asks for them.
+    At most ``capacity`` experts are kept (least recently used dropped first), so that
+    comparing every token of a 64-token batch does not hold ~220 experts (~77 GB in fp64)."""
+
+    def __init__(self, w, capacity=16):
+        self.w, self.capacity = w, capacity
+        self.cache = collections.OrderedDict()
 
     def __call__(self, e):
-        if e not in self.cache:
-            self.cache[e] = (f64(self.w["W_gate"][e]), f64(self.w["W_up"][e]), f64(self.w["W_down"][e]))
+        e = int(e)
+        if e in self.cache:
+            self.cache.move_to_end(e)
+        else:
+            while len(self.cache) >= self.capacity:
+                self.cache.popitem(last=False)
+            self.cache[e] = (f64_big(self.w["W_gate"][e]), f64_big(self.w["W_up"][e]),
+                             f64_big(self.w["W_down"][e]))
         return self.cache[e]
 
     def shared(self):
-        return [(f64(self.w["Ws_gate"][0]), f64(self.w["Ws_up"][0]), f64(self.w["Ws_down"][0]))]
+        return [(f64_big(self.w["Ws_gate"][s]), f64_big(self.w["Ws_up"][s]), f64_big(self.w["Ws_down"][s]))
+                for s in range(self.w["Ws_gate"].shape[0])]

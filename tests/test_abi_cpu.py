@@ -104,7 +104,13 @@ def test_kda_rejects_null_and_misaligned(lib):
 
 
 def test_spec_window_rejects_bad_phase_and_long_window(lib):
-    assert lib.kda_spec_verify_replay(3, 1, 4, 4, 64, 64, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE,
+    # BOTH is a named phase that no single call can serve (a window's acceptance depends on its
+    # own verify outputs): unsupported, not an invalid argument
+    assert lib.kda_spec_verify_replay(hla.HLA_SPEC_BOTH, 1, 4, 4, 64, 64, FAKE, None, FAKE, FAKE,
+                                      FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == 2
+    assert lib.kda_spec_verify_replay(4, 1, 4, 4, 64, 64, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                      FAKE, FAKE, 0, None) == 1
+    assert lib.kda_spec_verify_replay(0, 1, 4, 4, 64, 64, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE,
                                       FAKE, FAKE, 0, None) == 1
     assert lib.kda_spec_verify_replay(1, 1, 9, 4, 64, 64, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE,
                                       None, FAKE, 0, None) == 2

@@ -1,6 +1,6 @@
 """The full hybrid decode layer (hidden 7168, 32 KDA heads of 128, 256 experts top-8 + 1
-shared) through the C-ABI executor, against the oracle's composed layer on sampled
-sequences (each sequence's layer output depends only on its own token and state)."""
+shared) through the C-ABI executor, against the oracle's composed layer on every sequence
+(a sequence whose router logits hold a near tie is compared on its state only)."""
 
 import numpy as np
 import pytest
@@ -14,7 +14,7 @@ from tests.gpu_common import (FULL, LAYER_FROB_REL, ExpertCache, f64, frob_rel, 
 pytestmark = pytest.mark.gpu
 
 H, D = 32, 128
-ROUTER_MARGIN = 1e-3   # skip sampled tokens whose oracle top-(k+1) logits are closer than this
+ROUTER_MARGIN = 1e-3   # y is not compared for a token whose oracle top-(k+1) logits are closer than this
 
 
 @pytest.fixture(scope="module")
@@ -50,21 +50,20 @@ def test_decode_layer(dev, full_moe, layer, M):
     S = S0.to(dev)
     y = _run(dev, L, M, x.to(dev), S)
     torch.cuda.synchronize()
-    assert hla.hla_last_variant() == "decode_layer"
+    assert hla.hla_last_variant().startswith("decode_layer")
     cache = ExpertCache(full_moe)
-    checked = 0
-    for m in sorted(set([0, M // 2, M - 1, 1 % M, (M * 3) // 4])):
-        y_ref, S_ref, aux = oracle.layer.decode_layer(f64(x)[m:m + 1], f64(S0)[m:m + 1], p, cache,
-                                                       cache.shared())
-        top = np.sort(aux["logits"][0])[::-1][:FULL["k"] + 1]
+    y_ref, S_ref, aux = oracle.layer.decode_layer(f64(x), f64(S0), p, cache, cache.shared())
+    S_got, y_got = f64(S), f64(y)
+    ties = 0
+    for m in range(M):
+        # the state does not depend on the routing: every sequence
+        assert frob_rel(S_got[m], S_ref[m]) < LAYER_FROB_REL, m
+        top = np.sort(aux["logits"][m])[::-1][:FULL["k"] + 1]
         if np.any(-np.diff(top) < ROUTER_MARGIN):
+            ties += 1
             continue  # a near tie in routing: the two sides may legitimately pick differently
-        assert frob_rel(f64(y)[m:m + 1], y_ref) < LAYER_FROB_REL, m
-        assert frob_rel(f64(S)[m:m + 1], S_ref) < LAYER_FROB_REL, m
-        checked += 1
-        if checked == 3:
-            break
-    assert checked >= 1
+        assert frob_rel(y_got[m], y_ref[m]) < LAYER_FROB_REL, m
+    assert ties <= M // 4, ties
 
 
 @pytest.mark.parametrize("M,mask", [(8, "7"), (64, None), (64, "7")])
@@ -139,3 +138,39 @@ def test_layer_shared_experts_on_side_stream(dev, layer, M, monkeypatch):
     torch.cuda.synchronize()
     assert torch.equal(y, y_side) and torch.equal(S_graph, S_side)
 
+
+
+@pytest.mark.parametrize("M", [1, 8, 64])
+def test_layer_programmatic_launch_is_bitwise_neutral(dev, layer, M, monkeypatch):
+    """The layer's kernels chained by programmatic dependent launch (each loads its weights or
+    state before waiting for its predecessor) give the same bits as plain launches, eager and
+    captured in a CUDA graph with the prefetch stream."""
+    w, L, p = layer
+    x = inputs.activations(M, FULL["Hd"], inputs.generator(4600 + M)).to(dev)
+    S0 = warm_states(4, M, H, D)
+    out = {}
+    for mode in ("0", "1"):
+        monkeypatch.setenv("HLA_PDL", mode)
+        S = S0.to(dev)
+        y = _run(dev, L, M, x, S, prefetch=True)
+        out[mode] = (y, S, hla.hla_last_variant())
+    torch.cuda.synchronize()
+    assert "<pdl>" in out["1"][2] and "<pdl>" not in out["0"][2]
+    assert torch.equal(out["0"][0], out["1"][0]) and torch.equal(out["0"][1], out["1"][1])
+    monkeypatch.setenv("HLA_PDL", "1")
+    y = torch.empty(M, FULL["Hd"], dtype=torch.bfloat16, device=dev)
+    nb = hla.hla_decode_layer_workspace_size(L, M)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream()
+    S_graph = S0.to(dev)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            hla.hla_decode_layer(L, M, x, S_graph, None, y, ws, nb, prefetch_stream=side)
+    for _ in range(2):  # replays after the first see the previous replay's workspace contents
+        S_graph.copy_(S0.to(dev))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, out["0"][0]) and torch.equal(S_graph, out["0"][1])
