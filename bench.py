@@ -169,6 +169,24 @@ def barrier(world):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+class launch_chain:
+    """Brackets library calls queued back to back on the current stream as one launch chain
+    (hla_chain_begin / hla_chain_end) unless HLA_BENCH_CHAIN=0."""
+
+    def __init__(self, hla):
+        self.hla = hla
+        self.on = os.environ.get("HLA_BENCH_CHAIN", "1") == "1"
+
+    def __enter__(self):
+        if self.on:
+            self.hla.hla_chain_begin()
+
+    def __exit__(self, *exc):
+        if self.on:
+            self.hla.hla_chain_end()
+        return False
+
+
 class Workload:
     """Device-resident weights, states, rotating inputs and workspaces of one step."""
 
@@ -221,13 +239,15 @@ class Workload:
         win = self.win[r] if win is None else win
         dr, tg = (self.ids[r][0], self.ids[r][1]) if ids is None else ids
         B, T, H, d = c["spec_B"], c["spec_T"], c["H"], c["d"]
-        hla.hla_decode_layer(self.L, c["M"], x, self.S, None, self.y, self.ws, self.ws_bytes,
-                             prefetch_stream=self.side)
-        hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, self.S_spec, None, win["q"],
-                                   win["k"], win["v"], win["alpha"], win["beta"], None, self.o_spec)
-        hla.spec_accept_prefix(B, T, dr, tg, self.acc, self.com)
-        hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, self.S_spec, None, win["q"],
-                                   win["k"], win["v"], win["alpha"], win["beta"], self.acc, None)
+        # one launch chain: the layer's kernels, then the window's, back to back on this stream
+        with launch_chain(hla):
+            hla.hla_decode_layer(self.L, c["M"], x, self.S, None, self.y, self.ws, self.ws_bytes,
+                                 prefetch_stream=self.side)
+            hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, self.S_spec, None, win["q"],
+                                       win["k"], win["v"], win["alpha"], win["beta"], None, self.o_spec)
+            hla.spec_accept_prefix(B, T, dr, tg, self.acc, self.com)
+            hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, self.S_spec, None, win["q"],
+                                       win["k"], win["v"], win["alpha"], win["beta"], self.acc, None)
 
     def active_experts(self):
         torch = self.torch
@@ -408,19 +428,21 @@ def spec_sweep(torch, hla, inputs, wl, dev, peak):
         def separate(i, B=B, wins=wins, ids=ids, o=o, acc=acc, com=com, idxs=idxs):
             w = wins[i % ROTATE]
             dr, tg, _ = ids[i % ROTATE]
-            hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, pool, idxs[i], w["q"], w["k"],
-                                       w["v"], w["alpha"], w["beta"], None, o)
-            hla.spec_accept_prefix(B, T, dr, tg, acc, com)
-            hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, pool, idxs[i], w["q"], w["k"],
-                                       w["v"], w["alpha"], w["beta"], acc, None)
+            with launch_chain(hla):
+                hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, pool, idxs[i], w["q"], w["k"],
+                                           w["v"], w["alpha"], w["beta"], None, o)
+                hla.spec_accept_prefix(B, T, dr, tg, acc, com)
+                hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, pool, idxs[i], w["q"], w["k"],
+                                           w["v"], w["alpha"], w["beta"], acc, None)
 
         def fused(i, B=B, wins=wins, ids=ids, o=o, acc=acc, com=com, idxs=idxs):
             p_, w = wins[(i + ROTATE - 1) % ROTATE], wins[i % ROTATE]
             dr, tg, _ = ids[i % ROTATE]
-            hla.kda_spec_replay_verify(B, T, T, H, d, d, pool, idxs[i], p_["q"], p_["k"], p_["v"],
-                                       p_["alpha"], p_["beta"], acc, w["q"], w["k"], w["v"],
-                                       w["alpha"], w["beta"], o)
-            hla.spec_accept_prefix(B, T, dr, tg, acc, com)
+            with launch_chain(hla):
+                hla.kda_spec_replay_verify(B, T, T, H, d, d, pool, idxs[i], p_["q"], p_["k"], p_["v"],
+                                           p_["alpha"], p_["beta"], acc, w["q"], w["k"], w["v"],
+                                           w["alpha"], w["beta"], o)
+                hla.spec_accept_prefix(B, T, dr, tg, acc, com)
         mean_sep = statistics.mean(sum(spec_bytes(B, T, ids[r][2]).values()) for r in range(ROTATE))
         mean_fused = statistics.mean(
             B * H * 4 * d * d + sum(H * (4 * d * d + int(a) * tok) for a in ids[r][2] if a > 0)
@@ -904,6 +926,46 @@ def run_layer_ab(spec, reps=5, batches=(1, 2, 8, 32, 64)):
     print(json.dumps({"layer_ab_us_per_call": table, "switch": var, "reps": reps, "clocks": clocks}))
 
 
+def run_spec_ab(spec, reps=3):
+    """The speculative-window sweep (B = 16 and 64, separate and fused forms, states rotated past
+    L2) for each value of one tuning switch, e.g. ``HLA_KDA_STREAM=0,1``; repetitions interleaved.
+    One JSON line with the median microseconds and fractions of the peak."""
+    import torch
+    from hybrid_linear_attention_gated_gb300 import build, hla, inputs
+    var, vals = spec.split("=")
+    vals = vals.split(",")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    peak, _ = peaks()
+
+    class _Wl:  # the spec sweep needs only the B=16 windows
+        pass
+    wl = _Wl()
+    g = inputs.generator(5, dev)
+    wl.win, wl.ids = [], []
+    for _ in range(ROTATE):
+        wl.win.append(inputs.kda_inputs((CFG["spec_B"], CFG["spec_T"]), CFG["H"], CFG["d"], CFG["d"], g, dev))
+        dr, tg, a = inputs.accept_ids(CFG["spec_B"], CFG["spec_T"], g, dev)
+        wl.ids.append((dr, tg, a.cpu().numpy()))
+    sampler = ClockSampler(0)
+    sampler.start()
+    res = {v: [] for v in vals}
+    for _ in range(reps):
+        for v in vals:
+            os.environ[var] = v
+            res[v].append(spec_sweep(torch, hla, inputs, wl, dev, peak))
+    os.environ.pop(var, None)
+    clocks = sampler.stop()
+    table = {}
+    for v, runs in res.items():
+        for i, row in enumerate(runs[0]):
+            us = statistics.median(r[i]["us"] for r in runs)
+            key = f"B{row['batch']}_{row['form']}"
+            table.setdefault(key, {})[v] = dict(us=round(us, 2), frac=round(row["bytes"] / us / 1e3 / peak, 3))
+    print(json.dumps({"spec_ab": table, "switch": var, "reps": reps, "clocks": clocks}))
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -1000,6 +1062,8 @@ def main():
                     help="time the layer under every side-stream prefetch mask and exit")
     ap.add_argument("--layer-ab", metavar="VAR=v1,v2",
                     help="time the layer at batch 1-64 for each value of one tuning switch and exit")
+    ap.add_argument("--spec-ab", metavar="VAR=v1,v2",
+                    help="time the speculative window for each value of one tuning switch and exit")
     args = ap.parse_args()
     if args.profile:
         return run_profile(args.profile)
@@ -1007,6 +1071,8 @@ def main():
         return run_prefetch_ab()
     if args.layer_ab:
         return run_layer_ab(args.layer_ab)
+    if args.spec_ab:
+        return run_spec_ab(args.spec_ab)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

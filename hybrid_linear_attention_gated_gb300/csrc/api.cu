@@ -44,21 +44,40 @@ void trace_after(int kernel, cudaStream_t st) {
 }
 
 namespace {
-thread_local bool g_pdl_on = false;
-thread_local cudaStream_t g_pdl_stream = nullptr;
+thread_local bool g_pdl_on = false;         // a chain is open ...
+thread_local cudaStream_t g_pdl_stream = nullptr;  // ... on this stream
+thread_local bool g_pdl_started = false;    // and a kernel of it has been launched
 }  // namespace
 
-PdlChain::PdlChain(cudaStream_t st, bool on) : prev_on(g_pdl_on), prev_st(g_pdl_stream) {
+PdlChain::PdlChain(cudaStream_t st, bool on)
+    : prev_on(g_pdl_on), prev_started(g_pdl_started), prev_st(g_pdl_stream) {
+    // inside a chain already open on this stream, the first kernel follows that chain's last
+    const bool continues = g_pdl_on && g_pdl_stream == st && g_pdl_started;
     g_pdl_on = on;
     g_pdl_stream = st;
+    g_pdl_started = continues;
 }
 
 PdlChain::~PdlChain() {
+    const bool launched_inside = g_pdl_started;
+    const bool same_stream = g_pdl_stream == prev_st;
     g_pdl_on = prev_on;
     g_pdl_stream = prev_st;
+    // an outer chain on the same stream goes on after the kernels queued inside this one
+    g_pdl_started = prev_started || (same_stream && launched_inside);
 }
 
-bool pdl_for(cudaStream_t st) { return g_pdl_on && st == g_pdl_stream; }
+bool pdl_for(cudaStream_t st) { return g_pdl_on && g_pdl_started && st == g_pdl_stream; }
+
+// records that a kernel went out on the chain's stream (chained or not)
+void pdl_launched(cudaStream_t st) {
+    if (st == g_pdl_stream) g_pdl_started = true;
+}
+
+namespace {
+// the chain a caller opened with hla_chain_begin (at most one per host thread)
+thread_local PdlChain *g_user_chain = nullptr;
+}  // namespace
 
 int prefetch_mask() {
     const char *env = getenv("HLA_PREFETCH_MASK");
@@ -94,6 +113,19 @@ extern "C" const char *hla_status_string(int status) {
 extern "C" const char *hla_last_variant(void) { return g_variant; }
 
 extern "C" int hla_version(void) { return 100; }
+
+extern "C" int hla_chain_begin(hla_stream stream) {
+    if (hla::g_user_chain) return HLA_ERR_INVALID_ARG;  // already open on this thread
+    hla::g_user_chain = new hla::PdlChain((cudaStream_t)stream, true);
+    return HLA_OK;
+}
+
+extern "C" int hla_chain_end(void) {
+    if (!hla::g_user_chain) return HLA_ERR_INVALID_ARG;
+    delete hla::g_user_chain;
+    hla::g_user_chain = nullptr;
+    return HLA_OK;
+}
 
 extern "C" unsigned long long hla_launch_count(void) {
     return g_launches.load(std::memory_order_relaxed);

@@ -54,21 +54,28 @@ enum { kPrefetchLayer = 1, kPrefetchSharedGateUp = 2, kPrefetchSharedDown = 4 };
 int prefetch_mask();
 
 // ----------------------------------------------------------------------------- launch chains
-// Programmatic dependent launch.  Inside a chain (the decode layer's main stream, see
-// PdlChain) every kernel after the first is launched with programmatic stream serialisation:
-// it may start while its predecessor still runs, does the work that does not depend on the
-// predecessor (e.g. loading static weights or its own state), then waits (pdl_wait) until the
-// predecessor has completed and its writes are visible.  Each kernel lets its successor start
-// (pdl_trigger) only after its own wait, so when a kernel starts, every kernel before its
-// immediate predecessor has completed: its pre-wait reads may touch anything the immediate
-// predecessor does not write.  Outside a chain every launch is plain and pdl_wait is a no-op.
+// Programmatic dependent launch.  Inside a chain (the decode layer's main stream, or calls a
+// caller brackets with hla_chain_begin / hla_chain_end) every kernel after the chain's first is
+// launched with programmatic stream serialisation: it may start while its predecessor still
+// runs, does the work that does not depend on the predecessor (e.g. loading static weights or
+// its own state), then waits (pdl_wait) until the predecessor has completed and its writes are
+// visible.  Each kernel lets its successor start (pdl_trigger) only after its own wait, so when a
+// kernel starts, every kernel before its immediate predecessor has completed: its pre-wait
+// reads may touch anything the immediate predecessor does not write.  Every kernel of the
+// library keeps to that, so any sequence of library kernels can form a chain.  Outside a chain
+// every launch is plain and pdl_wait is a no-op.
+//
+// A PdlChain object opens a chain on a stream for its lifetime.  Inside a chain already open on
+// the same stream it continues that chain (its first kernel follows the outer chain's last);
+// otherwise its first kernel is launched plain, after whatever the caller queued before.
 struct PdlChain {
     PdlChain(cudaStream_t st, bool on);
     ~PdlChain();
-    bool prev_on;
+    bool prev_on, prev_started;
     cudaStream_t prev_st;
 };
-bool pdl_for(cudaStream_t st);  // launch with programmatic serialisation on this stream?
+bool pdl_for(cudaStream_t st);       // launch with programmatic serialisation on this stream?
+void pdl_launched(cudaStream_t st);  // a kernel was launched on st (the chain has started)
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -83,7 +90,9 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_for(st) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e == cudaSuccess) pdl_launched(st);
+    return e;
 }
 
 #define HLA_REQUIRE(cond, status) \
@@ -122,6 +131,63 @@ __device__ __forceinline__ uint4 ld_weight_v4(const void *p) {
 // Plain coherent 128-bit load for activations / states.
 __device__ __forceinline__ uint4 ld_act_v4(const void *p) {
     return *reinterpret_cast<const uint4 *>(p);
+}
+
+// ----------------------------------------------------------------------------- async copies
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Wait until the phase with the given parity completes, for at most limit_ns of %globaltimer.
+// Returns false (after writing HLA_ERR_DEVICE_TIMEOUT to *status) if it has not by then.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                              int *status) {
+    const uint32_t a = smem_u32(bar);
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((i & 63) == 0) {  // the clock is read every 64 polls
+            const uint64_t t = global_ns();
+            if (i == 0) t0 = t;
+            else if (t - t0 > limit_ns) break;
+        }
+    }
+    atomicExch(status, HLA_ERR_DEVICE_TIMEOUT);
+    return false;
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global memory
+// into this CTA's shared memory, completing on the mbarrier's transaction count.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
 }
 
 // D(16x8 fp32) += A(16x16 bf16, row) * B(16x8 bf16, col)

@@ -508,6 +508,9 @@ __global__ void __launch_bounds__(kRouterThreads)
 }
 
 __global__ void l2_prefetch_kernel(const char *p, size_t bytes, uint32_t chunk) {
+    // it reads only static weights, but in a launch chain a kernel must not let its successor
+    // start before its own predecessor has completed
+    pdl_wait_trigger();
     const size_t stride = (size_t)gridDim.x * blockDim.x * chunk;
     for (size_t off = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) * chunk; off < bytes;
          off += stride) {
@@ -629,8 +632,8 @@ int run_l2_prefetch(const void *ptr, size_t bytes, cudaStream_t st) {
     long threads = (long)((bytes + chunk - 1) / chunk);
     int blocks = (int)((threads + 127) / 128);
     if (blocks > sm_count()) blocks = sm_count();
-    l2_prefetch_kernel<<<blocks, 128, 0, st>>>(reinterpret_cast<const char *>(ptr), bytes, chunk);
-    return launch_status();
+    return launched(launch_kernel(l2_prefetch_kernel, dim3(blocks), dim3(128), 0, st,
+                                  reinterpret_cast<const char *>(ptr), bytes, chunk));
 }
 
 int run_qkvg(int M, int Hd, int H, int d, const hla_bf16 *x, const hla_bf16 *W, hla_bf16 *q,

@@ -128,11 +128,12 @@ extern "C" int hla_decode_layer(const hla_layer *L, int M, const hla_bf16 *x, fl
     cudaStream_t st = (cudaStream_t)stream, pf = (cudaStream_t)prefetch_stream;
     int r;
 
-    if ((r = hla_rmsnorm(M, Hd, x, L->gamma_attn, L->eps, bf(lo.x1), stream)) != HLA_OK) return r;
-    // Every later kernel on `stream` is a programmatic dependent of the one before it (the first
-    // is a plain launch, after whatever the caller queued): it loads its static weights or its
-    // state while its predecessor finishes.  Side-stream launches stay plain.
+    // Every kernel on `stream` after the first is a programmatic dependent of the one before it:
+    // it loads its static weights or its state while its predecessor finishes.  The first is a
+    // plain launch after whatever the caller queued (or, inside a chain the caller opened, the
+    // next link of that chain).  Side-stream launches stay plain.
     const PdlChain chain(st, layer_pdl(M));
+    if ((r = hla_rmsnorm(M, Hd, x, L->gamma_attn, L->eps, bf(lo.x1), stream)) != HLA_OK) return r;
     if ((r = kda_qkvg_proj(M, Hd, H, d, d, bf(lo.x1), L->W_qkvgb, bf(lo.q), bf(lo.k), bf(lo.v),
                            f32(lo.alpha), f32(lo.beta), 0, w + lo.qkvg_ws, lo.qkvg_bytes,
                            stream)) != HLA_OK)

@@ -54,49 +54,11 @@ __device__ int g_tc_status = 0;
 // CTA then returns before it allocates tensor memory or issues a copy or an MMA.
 std::atomic<int> g_force_timeout{0};
 
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
 // Wait for the phase with the given parity for at most limit_ns of %globaltimer; false (and
 // the status word set) if it has not completed by then.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           uint64_t limit_ns = kWaitLimitNs) {
-    const uint32_t a = smem_u32(bar);
-    uint64_t t0 = 0;
-    for (uint32_t i = 0;; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(a), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((i & 63) == 0) {  // the clock is read every 64 polls
-            const uint64_t t = global_ns();
-            if (i == 0) t0 = t;
-            else if (t - t0 > limit_ns) break;
-        }
-    }
-    atomicExch(&g_tc_status, HLA_ERR_DEVICE_TIMEOUT);
-    return false;
+    return mbar_wait_for(bar, parity, limit_ns, &g_tc_status);
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,

@@ -46,6 +46,8 @@ SIGNATURES = {
     "hla_status_string": (c_char_p, [c_int]),
     "hla_last_variant": (c_char_p, []),
     "hla_version": (c_int, []),
+    "hla_chain_begin": (c_int, [P]),
+    "hla_chain_end": (c_int, []),
     "kda_decode_step": (c_int, [c_int] * 4 + [P] * 8 + [c_int, P]),
     "kda_spec_verify_replay": (c_int, [c_int] * 6 + [P] * 9 + [c_int, P]),
     "spec_accept_prefix": (c_int, [c_int, c_int] + [P] * 4 + [P]),
@@ -135,6 +137,14 @@ def hla_last_variant():
 
 def hla_version():
     return load().hla_version()
+
+
+def hla_chain_begin(stream=None):
+    return _check("hla_chain_begin", load().hla_chain_begin(_stream(stream)))
+
+
+def hla_chain_end():
+    return _check("hla_chain_end", load().hla_chain_end())
 
 
 def kda_decode_step(B, H, dk, dv, S, state_idx, q, k, v, alpha, beta, o, o_dtype=HLA_F32,

@@ -93,6 +93,24 @@ const char *hla_last_variant(void);
 int hla_version(void);
 
 /* ---------------------------------------------------------------------------
+ * Launch chains.  No counterpart on the source pages: a scheduling contract for callers that
+ * queue several library calls back to back (a decode step: the layer, then the speculative
+ * window's verify, accept and replay).
+ * hla_chain_begin(stream) declares that the library calls this host thread makes on `stream`
+ * until hla_chain_end() follow one another with nothing else queued on that stream between
+ * them (no kernel, copy or event of the caller's).  Every kernel of those calls after the
+ * chain's first is then launched as a programmatic dependent of the one before it: it may
+ * start while its predecessor finishes, loads only data its predecessor does not write (static
+ * weights, its own state) and waits for the predecessor before reading anything else.  Results
+ * are bit-identical to plain launches.  Side streams are not part of the chain.  One chain per
+ * host thread: a second hla_chain_begin, or hla_chain_end without one, returns
+ * HLA_ERR_INVALID_ARG.  hla_decode_layer chains its own kernels at up to 32 tokens and, inside a
+ * caller's chain on the same stream, continues it.
+ * -------------------------------------------------------------------------*/
+int hla_chain_begin(hla_stream stream);
+int hla_chain_end(void);
+
+/* ---------------------------------------------------------------------------
  * KDA decode step.  [KIMI-WEBINAR] fixed-size recurrent state; [VLLM-K3]
  * Part 1 sec. 1, KDA decode kernel tuned to batch size and heads.
  *

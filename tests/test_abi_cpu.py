@@ -149,3 +149,12 @@ def test_oracle_is_not_on_the_product_path():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
+
+
+def test_launch_chain_rules(lib):
+    """One chain per host thread; hla_chain_end needs an open chain (no CUDA call is made)."""
+    assert lib.hla_chain_end() == 1
+    assert lib.hla_chain_begin(None) == 0
+    assert lib.hla_chain_begin(None) == 1
+    assert lib.hla_chain_end() == 0
+    assert lib.hla_chain_end() == 1

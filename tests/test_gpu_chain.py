@@ -1,0 +1,79 @@
+"""Launch chains (hla_chain_begin / hla_chain_end): library calls queued back to back on one
+stream, every kernel after the first a programmatic dependent of the one before it, must give
+the bits of plain launches."""
+
+import pytest
+import torch
+
+from hybrid_linear_attention_gated_gb300 import hla, inputs
+from tests.gpu_common import require_gpu, warm_states
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_gpu()
+
+
+def _to(d, dev):
+    return {k: v.to(dev) for k, v in d.items()}
+
+
+def _spec_window(B, T, H, d, S, win, dr, tg, acc, com, o):
+    hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, S, None, win["q"], win["k"],
+                               win["v"], win["alpha"], win["beta"], None, o)
+    hla.spec_accept_prefix(B, T, dr, tg, acc, com)
+    hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, S, None, win["q"], win["k"],
+                               win["v"], win["alpha"], win["beta"], acc, None)
+
+
+@pytest.mark.parametrize("B", [16, 64])
+def test_launch_chain_is_bitwise_neutral(dev, B):
+    """verify -> accept -> replay queued as one launch chain (each kernel a programmatic
+    dependent of the one before it) gives the bits of plain launches, eager and in a CUDA graph,
+    two windows in a row."""
+    T, H, d = 4, 32, 128
+    S0 = warm_states(8, B, H, d).to(dev)
+    g = inputs.generator(4700 + B)
+    wins = [_to(inputs.kda_inputs((B, T), H, d, d, g), dev) for _ in range(2)]
+    ids = [inputs.accept_ids(B, T, g) for _ in range(2)]
+    ids = [(dr.to(dev), tg.to(dev)) for dr, tg, _ in ids]
+
+    def run(chain, graph=False):
+        S = S0.clone()
+        acc = torch.zeros(B, dtype=torch.int32, device=dev)
+        com = torch.zeros(B, dtype=torch.int32, device=dev)
+        os_ = [torch.empty(B, T, H, d, device=dev) for _ in range(2)]
+
+        def body():
+            for w, (dr, tg), o in zip(wins, ids, os_):
+                if chain:
+                    hla.hla_chain_begin()
+                try:
+                    _spec_window(B, T, H, d, S, w, dr, tg, acc, com, o)
+                finally:
+                    if chain:
+                        hla.hla_chain_end()
+        if graph:
+            body()  # warm-up outside the capture
+            S.copy_(S0)
+            com.zero_()
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(gr, stream=s):
+                    body()
+            S.copy_(S0)
+            com.zero_()
+            gr.replay()
+        else:
+            body()
+        torch.cuda.synchronize()
+        return S, os_, acc, com
+
+    ref = run(False)
+    for got in (run(True), run(True, graph=True)):
+        assert torch.equal(got[0], ref[0]) and torch.equal(got[2], ref[2]) and torch.equal(got[3], ref[3])
+        assert all(torch.equal(a, b) for a, b in zip(got[1], ref[1]))
