@@ -40,6 +40,8 @@ sys.path.insert(0, ROOT)
 METRIC = "decode µs/step and achieved HBM GB/s (KDA + MoE) vs GB300 peak at batch 1–64"
 CFG = dict(M=64, Hd=7168, H=32, d=128, E=256, k=8, I=2048, n_shared=1, eps=1e-6,
            spec_B=16, spec_T=4)
+# draft length of the spec sweep's windows (the headline step keeps spec_T = 4)
+SWEEP_T = int(os.environ.get("HLA_BENCH_SPEC_T", "4"))
 ROTATE = 4  # distinct input batches cycled through the timed steps
 
 
@@ -402,13 +404,13 @@ def spec_sweep(torch, hla, inputs, wl, dev, peak):
     (> 3x L2) through state_idx, so every step reads its states from HBM; the inputs rotate
     through 4 windows.  tokens/s counts accepted tokens."""
     c = CFG
-    T, H, d = c["spec_T"], c["H"], c["d"]
+    T, H, d = SWEEP_T, c["H"], c["d"]
     tok = 3 * d * 2 + d * 4 + 4
     pool_slots = 768 * 2 ** 20 // (H * d * d * 4)
     pool = torch.randn(pool_slots, H, d, d, device=dev).mul_(0.05)
     res = []
     for B in (16, 64):
-        if B == c["spec_B"]:
+        if B == c["spec_B"] and T == c["spec_T"]:
             wins, ids = wl.win, wl.ids
         else:
             g = inputs.generator(7700 + B, dev)
@@ -889,8 +891,9 @@ def run_prefetch_ab(reps=4):
 
 def run_layer_ab(spec, reps=5, batches=(1, 2, 8, 32, 64)):
     """Layer time (CUDA graph of 8 calls, with the prefetch stream) at several batch sizes for
-    each value of one tuning switch, e.g. ``HLA_PDL=0,1``; repetitions are interleaved so that
-    the values see the same clocks.  One JSON line with the medians and the clocks."""
+    each value of one tuning switch, e.g. ``HLA_PDL=0,1`` (``-`` = the switch unset); repetitions
+    are interleaved so that the values see the same clocks.  One JSON line with the medians and
+    the clocks."""
     import torch
     from hybrid_linear_attention_gated_gb300 import build, hla, inputs
     var, vals = spec.split("=")
@@ -910,14 +913,24 @@ def run_layer_ab(spec, reps=5, batches=(1, 2, 8, 32, 64)):
         if S is None:
             continue
         y = torch.empty(M, c["Hd"], dtype=torch.bfloat16, device=dev)
-        nb = hla.hla_decode_layer_workspace_size(wl.L, M)
-        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+
+        def set_switch(v):
+            if v == "-":
+                os.environ.pop(var, None)
+            else:
+                os.environ[var] = v
+        nbs = {}
+        for v in vals:  # a switch may change the workspace size (e.g. a forced split)
+            set_switch(v)
+            nbs[v] = hla.hla_decode_layer_workspace_size(wl.L, M)
+        ws = torch.empty(max(nbs.values()), dtype=torch.uint8, device=dev)
         res = {v: [] for v in vals}
         for _ in range(reps):
             for v in vals:
-                os.environ[var] = v
+                set_switch(v)
+                nb = nbs[v]
 
-                def fn(i):
+                def fn(i, nb=nb):
                     hla.hla_decode_layer(wl.L, M, xs[i % ROTATE], S, None, y, ws, nb, prefetch_stream=wl.side)
                 res[v].append(graph_time(torch, fn, 8) * 1e6)
         os.environ.pop(var, None)
@@ -1062,6 +1075,7 @@ def main():
                     help="time the layer under every side-stream prefetch mask and exit")
     ap.add_argument("--layer-ab", metavar="VAR=v1,v2",
                     help="time the layer at batch 1-64 for each value of one tuning switch and exit")
+    ap.add_argument("--ab-batches", default="1,2,8,32,64", help="batch sizes of --layer-ab")
     ap.add_argument("--spec-ab", metavar="VAR=v1,v2",
                     help="time the speculative window for each value of one tuning switch and exit")
     args = ap.parse_args()
@@ -1070,7 +1084,7 @@ def main():
     if args.prefetch_ab:
         return run_prefetch_ab()
     if args.layer_ab:
-        return run_layer_ab(args.layer_ab)
+        return run_layer_ab(args.layer_ab, batches=tuple(int(b) for b in args.ab_batches.split(",")))
     if args.spec_ab:
         return run_spec_ab(args.spec_ab)
     if args.warmup < 3:

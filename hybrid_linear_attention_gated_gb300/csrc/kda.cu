@@ -50,6 +50,10 @@ struct KdaParams {
     void *o;
     int o_bf16;
     int B, T, Tp, H;
+    // the state may be read before waiting for the kernel before this one: set only where that
+    // kernel is known not to write the state (the decode layer's projection epilogue); inside a
+    // caller's launch chain the predecessor may be a KDA kernel that writes it
+    int state_first;
 };
 
 // Each CTA runs a short program over its (sequence, head, column slice):
@@ -100,11 +104,11 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4, kda_min_blocks(CW, MODE))
     const int b = bh / p.H;
     const int col0 = slice * CW;
 
-    // Decode and verify read their state slice before waiting for the kernel before them (in a
-    // launch chain that kernel produces the tokens, never the state); the other programs first
-    // read accepted lengths or sequence offsets, which the kernel before them may write.
-    constexpr bool STATE_FIRST = MODE == kDecode || MODE == kVerify;
-    if (!STATE_FIRST) pdl_wait_trigger();
+    // Decode and verify may read their state slice before waiting for the kernel before them,
+    // when the caller knows that kernel does not write the state (p.state_first); otherwise, and
+    // for the programs that first read accepted lengths or sequence offsets, they wait first.
+    const bool state_first = (MODE == kDecode || MODE == kVerify) && p.state_first;
+    if (!state_first) pdl_wait_trigger();
 
     int n_pre = 0, n_main = MODE == kDecode ? 1 : p.T;
     int seq0 = 0;
@@ -154,7 +158,7 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4, kda_min_blocks(CW, MODE))
             *reinterpret_cast<float4 *>(Sb + (size_t)(rg + kRowGroups * j) * DV) =
                 make_float4(s[j][0].x, s[j][0].y, s[j][1].x, s[j][1].y);
     };
-    if (STATE_FIRST) pdl_wait_trigger();
+    if (state_first) pdl_wait_trigger();
 
     // Only extend programs can exceed one block of TMAX tokens; for the others the loop body
     // runs once with every step in it (and compiles to straight-line code).
@@ -377,7 +381,8 @@ struct PrevWindow {
 int run_kda(int mode, int B, int T, int H, int dk, int dv, float *S, const int32_t *state_idx,
             const hla_bf16 *q, const hla_bf16 *k, const hla_bf16 *v, const float *alpha,
             const float *beta, const int32_t *accepted, void *o, int o_dtype, cudaStream_t st,
-            const PrevWindow &prev = PrevWindow(), const int32_t *cu_seqlens = nullptr) {
+            const PrevWindow &prev = PrevWindow(), const int32_t *cu_seqlens = nullptr,
+            bool state_first = false) {
     HLA_REQUIRE(B >= 1 && H >= 1 && T >= 1, HLA_ERR_INVALID_ARG);
     HLA_REQUIRE(dk == dv && (dk == 64 || dk == 128), HLA_ERR_UNSUPPORTED);
     HLA_REQUIRE(T <= kMaxWindow, HLA_ERR_UNSUPPORTED);
@@ -407,6 +412,7 @@ int run_kda(int mode, int B, int T, int H, int dk, int dv, float *S, const int32
     p.Tp = prev.T;
     p.accepted = accepted; p.o = o; p.o_bf16 = o_dtype == HLA_BF16; p.B = B; p.T = T; p.H = H;
     p.cu_seqlens = cu_seqlens;
+    p.state_first = state_first ? 1 : 0;
     int cw = choose_cw(B, H, dv, mode);
     if (mode == kReplayVerify && cw > 64) cw = 64;  // two windows of token vectors in shared memory
     static const char *names[5] = {"decode", "verify", "replay", "replay_verify", "extend"};
@@ -441,6 +447,16 @@ __global__ void accept_prefix_kernel(int B, int T, const int32_t *__restrict__ d
 }
 
 }  // namespace
+
+// The decode layer's KDA step: its stream predecessor is the input projection's epilogue, which
+// does not write the state, so the state slice is loaded before waiting for it.
+int kda_decode_step_in_layer(int B, int H, int dk, float *S, const int32_t *state_idx, const hla_bf16 *q,
+                             const hla_bf16 *k, const hla_bf16 *v, const float *alpha, const float *beta,
+                             void *o, int o_dtype, cudaStream_t st) {
+    return run_kda(kDecode, B, 1, H, dk, dk, S, state_idx, q, k, v, alpha, beta, nullptr, o, o_dtype, st,
+                   PrevWindow(), nullptr, true);
+}
+
 }  // namespace hla
 
 using namespace hla;

@@ -94,6 +94,9 @@ bool layer_pdl(int M) {
 }  // namespace
 
 bool moe_shared_on_side(int M, int nsh, bool have_side);
+int kda_decode_step_in_layer(int B, int H, int dk, float *S, const int32_t *state_idx, const hla_bf16 *q,
+                             const hla_bf16 *k, const hla_bf16 *v, const float *alpha, const float *beta,
+                             void *o, int o_dtype, cudaStream_t st);
 int moe_shared_side(int M, int Hd, int I, int E, int k, int nsh, const hla_bf16 *x,
                     const hla_bf16 *Ws_gate, const hla_bf16 *Ws_up, const hla_bf16 *Ws_down,
                     void *ws, cudaStream_t st, cudaStream_t side);
@@ -152,8 +155,8 @@ extern "C" int hla_decode_layer(const hla_layer *L, int M, const hla_bf16 *x, fl
             return r;
         if (cudaEventRecord(ev->join, pf) != cudaSuccess) return HLA_ERR_CUDA;
     }
-    if ((r = kda_decode_step(M, H, d, d, S, state_idx, bf(lo.q), bf(lo.k), bf(lo.v), f32(lo.alpha),
-                             f32(lo.beta), bf(lo.o), HLA_BF16, stream)) != HLA_OK)
+    if ((r = kda_decode_step_in_layer(M, H, d, S, state_idx, bf(lo.q), bf(lo.k), bf(lo.v), f32(lo.alpha),
+                                      f32(lo.beta), bf(lo.o), HLA_BF16, st)) != HLA_OK)
         return r;
     if ((r = skinny_proj_residual_rmsnorm(M, Hd, H * d, bf(lo.o), L->W_o, x, L->gamma_moe, L->eps,
                                           bf(lo.r), bf(lo.x2), 0, w + lo.oproj_ws, lo.oproj_bytes,

@@ -102,8 +102,10 @@ int hla_version(void);
  * chain's first is then launched as a programmatic dependent of the one before it: it may
  * start while its predecessor finishes, loads only data its predecessor does not write (static
  * weights, its own state) and waits for the predecessor before reading anything else.  Results
- * are bit-identical to plain launches.  Side streams are not part of the chain.  One chain per
- * host thread: a second hla_chain_begin, or hla_chain_end without one, returns
+ * are bit-identical to plain launches.  What a kernel reads before its wait is the weights and
+ * norm gains of its own call: inside a chain these must not be written by the call right before
+ * it (weights are static in the decode loop).  Side streams are not part of the chain.  One chain
+ * per host thread: a second hla_chain_begin, or hla_chain_end without one, returns
  * HLA_ERR_INVALID_ARG.  hla_decode_layer chains its own kernels at up to 32 tokens and, inside a
  * caller's chain on the same stream, continues it.
  * -------------------------------------------------------------------------*/

@@ -77,3 +77,44 @@ def test_launch_chain_is_bitwise_neutral(dev, B):
     for got in (run(True), run(True, graph=True)):
         assert torch.equal(got[0], ref[0]) and torch.equal(got[2], ref[2]) and torch.equal(got[3], ref[3])
         assert all(torch.equal(a, b) for a, b in zip(got[1], ref[1]))
+
+
+def test_chain_of_calls_on_the_same_state(dev):
+    """Chained calls where a kernel's predecessor writes the very state it reads: two decode steps
+    in a row, and the replay of one window followed by the verify of the next.  A kernel must not
+    read its state before its wait here; the results are the bits of plain launches."""
+    B, T, H, d = 8, 4, 32, 128
+    S0 = warm_states(9, B, H, d).to(dev)
+    g = inputs.generator(4900)
+    steps = [_to(inputs.kda_inputs((B,), H, d, d, g), dev) for _ in range(3)]
+    wins = [_to(inputs.kda_inputs((B, T), H, d, d, g), dev) for _ in range(2)]
+    acc = torch.tensor([0, 1, 2, 3, 4, 4, 1, 2], dtype=torch.int32, device=dev)
+
+    def run(chain):
+        S = S0.clone()
+        outs = []
+        if chain:
+            hla.hla_chain_begin()
+        try:
+            for u in steps:
+                o = torch.empty(B, H, d, device=dev)
+                hla.kda_decode_step(B, H, d, d, S, None, u["q"], u["k"], u["v"], u["alpha"], u["beta"], o)
+                outs.append(o)
+            w0, w1 = wins
+            hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, S, None, w0["q"], w0["k"], w0["v"],
+                                       w0["alpha"], w0["beta"], acc, None)
+            o = torch.empty(B, T, H, d, device=dev)
+            hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, S, None, w1["q"], w1["k"], w1["v"],
+                                       w1["alpha"], w1["beta"], None, o)
+            outs.append(o)
+        finally:
+            if chain:
+                hla.hla_chain_end()
+        torch.cuda.synchronize()
+        return S, outs
+
+    S_ref, o_ref = run(False)
+    for _ in range(3):
+        S_c, o_c = run(True)
+        assert torch.equal(S_c, S_ref)
+        assert all(torch.equal(a, b) for a, b in zip(o_c, o_ref))
