@@ -811,6 +811,17 @@ def run_profile(kind, iters=3):
         info.update(B=B, T=T, accepted=a.tolist(), verify_bytes=spec_bytes(B, T, a.cpu().numpy())["verify"],
                     replay_bytes=spec_bytes(B, T, a.cpu().numpy())["replay"],
                     variant=[verify_variant, hla.hla_last_variant()])
+    elif kind == "extend":
+        # four 512-token prefill chunks through kda_extend: each (sequence, head) is one serial
+        # chain of 512 steps (8 MB of state; the kernel is bound by its step latency, not HBM)
+        B, L, H, d = 4, 512, c["H"], c["d"]
+        S = torch.randn(B, H, d, d, device=dev).mul_(0.05)
+        cu = torch.arange(0, (B + 1) * L, L, dtype=torch.int32, device=dev)
+        u = inputs.kda_inputs((B * L,), H, d, d, g, dev)
+        o = torch.empty(B * L, H, d, device=dev)
+        for _ in range(iters):
+            hla.kda_extend(B, cu, H, d, d, S, None, u["q"], u["k"], u["v"], u["alpha"], u["beta"], o)
+        info.update(B=B, tokens=B * L, variant=hla.hla_last_variant())
     elif kind in ("layer1", "layer8"):
         # the decode layer at batch 1 or 8 with the full-size weights: three warm-up calls, then
         # `iters` calls in the NVTX range "timed" (for an ncu launch list of the small-batch layer)
@@ -941,7 +952,8 @@ def run_layer_ab(spec, reps=5, batches=(1, 2, 8, 32, 64)):
 
 def run_spec_ab(spec, reps=3):
     """The speculative-window sweep (B = 16 and 64, separate and fused forms, states rotated past
-    L2) for each value of one tuning switch, e.g. ``HLA_KDA_STREAM=0,1``; repetitions interleaved.
+    L2) for each value of one tuning switch, e.g. ``HLA_KDA_CW=0,32`` (0: the default width);
+    repetitions interleaved.
     One JSON line with the median microseconds and fractions of the peak."""
     import torch
     from hybrid_linear_attention_gated_gb300 import build, hla, inputs
@@ -1069,7 +1081,7 @@ def main():
     ap.add_argument("--threads", type=int, default=0,
                     help="reference arm: host threads the oracle may use (0 = every core); the "
                          "BLAS thread count is fixed by its environment variables at start-up")
-    ap.add_argument("--profile", choices=["moe", "kda", "spec", "dense", "dense16", "layer1", "layer8"],
+    ap.add_argument("--profile", choices=["moe", "kda", "spec", "extend", "dense", "dense16", "layer1", "layer8"],
                     help="run one small case of a hot kernel (for ncu captures) and exit")
     ap.add_argument("--prefetch-ab", action="store_true",
                     help="time the layer under every side-stream prefetch mask and exit")

@@ -180,6 +180,20 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, ui
     return false;
 }
 
+// Per-thread asynchronous copies into shared memory (16 bytes through L2 only, or 4 bytes), in
+// commit groups; wait_group<N> returns once at most N of this thread's groups are still pending.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global memory
 // into this CTA's shared memory, completing on the mbarrier's transaction count.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {

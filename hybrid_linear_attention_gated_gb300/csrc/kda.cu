@@ -56,6 +56,40 @@ struct KdaParams {
     int state_first;
 };
 
+// Extend programs take their sequences in two classes: first those with more than one block of
+// TMAX tokens (serial chains), in batch order, then the others.  Returns the sequence at schedule
+// position r, computed by the whole block from the sequence offsets.  In batch order, chains that
+// come after many short programs start only once those have filled the SMs, and finish last,
+// several to an SM.  Kept out of line: inlined, it changed the register allocation of the token
+// loop and made long chains slower.
+template <int NTHR, int TMAX>
+__device__ __noinline__ int extend_sequence_at(int r, int B, const int32_t *cu) {
+    __shared__ int s_cnt[NTHR / 32];
+    __shared__ int s_seq;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    auto is_chain = [&](int j) { return j < B && cu[j + 1] - cu[j] > TMAX; };
+    int n_chain = 0;
+    for (int base = 0; base < B; base += NTHR) n_chain += __syncthreads_count(is_chain(base + tid));
+    // position of sequence j: its rank among the chains, or n_chain + its rank among the others
+    int before = 0;  // chains in earlier rounds
+    for (int base = 0; base < B; base += NTHR) {
+        const int j = base + tid;
+        const bool chain = is_chain(j);
+        const unsigned m = __ballot_sync(0xffffffffu, chain);
+        if (lane == 0) s_cnt[warp] = __popc(m);
+        __syncthreads();
+        int lp = before + __popc(m & ((1u << lane) - 1u)), round = 0;
+        for (int w = 0; w < NTHR / 32; ++w) {
+            lp += w < warp ? s_cnt[w] : 0;
+            round += s_cnt[w];
+        }
+        if (j < B && (chain ? lp : n_chain + (j - lp)) == r) s_seq = j;  // exactly one j matches
+        before += round;
+        __syncthreads();
+    }
+    return s_seq;
+}
+
 // Each CTA runs a short program over its (sequence, head, column slice):
 //   n_pre steps from the previous window, then commit the state (replay-verify only);
 //   n_main steps from this call's tokens, writing o (decode, verify, replay-verify, extend)
@@ -94,6 +128,16 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4, kda_min_blocks(CW, MODE))
     __shared__ float sb[TMAX];
     auto rowpos = [](int i) { return (i & 7) * PAD + (i >> 3); };
 
+    // Only extend programs can exceed one block of TMAX tokens.  They copy the next block's raw
+    // token vectors into shared memory (asynchronously, two buffers) while the current block runs,
+    // so a long serial chain never waits on global memory between blocks.
+    constexpr bool BLOCKED = MODE == kExtend;
+    // per token: DK/8 16-byte chunks of q, DK/8 of k, DK/4 of alpha and CW/8 of v; item x of a
+    // block is chunk x % PER_TOK of token x / PER_TOK
+    constexpr int QC = DK / 8, AC = DK / 4, VC = CW / 8, PER_TOK = 2 * QC + AC + VC;
+    __shared__ __align__(16) uint4 raw[BLOCKED ? 2 : 1][BLOCKED ? TMAX * PER_TOK : 1];
+    __shared__ float rawb[BLOCKED ? 2 : 1][BLOCKED ? TMAX : 1];
+
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int rg = lane >> 2;
@@ -101,7 +145,7 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4, kda_min_blocks(CW, MODE))
     const int slice = blockIdx.x % NSLICE;
     const int bh = blockIdx.x / NSLICE;
     const int h = bh % p.H;
-    const int b = bh / p.H;
+    int b = bh / p.H;
     const int col0 = slice * CW;
 
     // Decode and verify may read their state slice before waiting for the kernel before them,
@@ -124,6 +168,7 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4, kda_min_blocks(CW, MODE))
         }
     }
     if (MODE == kExtend) {
+        b = extend_sequence_at<NTHR, TMAX>(b, p.B, p.cu_seqlens);
         seq0 = p.cu_seqlens[b];
         n_main = p.cu_seqlens[b + 1] - seq0;
         if (n_main <= 0) return;  // no new tokens: the state is not touched
@@ -138,6 +183,53 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4, kda_min_blocks(CW, MODE))
         if (MODE == kExtend) return ((size_t)seq0 + tm) * p.H + h;
         return ((size_t)b * Tld + tm) * p.H + h;
     };
+
+    // global address of item x of the block starting at step t0
+    auto item_src = [&](int x, int t0) -> const void * {
+        const int tt = x / PER_TOK, c = x - tt * PER_TOK;
+        const int t = t0 + tt;
+        const bool pre = t < n_pre;
+        const size_t tok = token_row(t);
+        if (c < QC) return (pre ? p.qp : p.q) + tok * DK + 8 * c;
+        if (c < 2 * QC) return (pre ? p.kp : p.k) + tok * DK + 8 * (c - QC);
+        if (c < 2 * QC + AC) return (pre ? p.alphap : p.alpha) + tok * DK + 4 * (c - 2 * QC);
+        return (pre ? p.vp : p.v) + tok * DV + col0 + 8 * (c - 2 * QC - AC);
+    };
+    // item x (16 bytes) into the staged layout: q, k and alpha row-group-major as fp32, v as fp32
+    auto store_item = [&](int x, const uint4 w) {
+        const int tt = x / PER_TOK, c = x - tt * PER_TOK;
+        if (c < 2 * QC + AC && c >= 2 * QC) {  // 4 alphas (fp32 bits), rows i0..i0+3
+            const int i0 = 4 * (c - 2 * QC);
+            sa[tt][rowpos(i0 + 0)] = __uint_as_float(w.x);
+            sa[tt][rowpos(i0 + 1)] = __uint_as_float(w.y);
+            sa[tt][rowpos(i0 + 2)] = __uint_as_float(w.z);
+            sa[tt][rowpos(i0 + 3)] = __uint_as_float(w.w);
+        } else if (c < 2 * QC) {  // 8 bf16 of q or k, rows 8j .. 8j+7 (one per row group)
+            float *dst = c < QC ? sq[tt] : sk[tt];
+            const int j = c < QC ? c : c - QC;
+            dst[0 * PAD + j] = bf16_lo(w.x); dst[1 * PAD + j] = bf16_hi(w.x);
+            dst[2 * PAD + j] = bf16_lo(w.y); dst[3 * PAD + j] = bf16_hi(w.y);
+            dst[4 * PAD + j] = bf16_lo(w.z); dst[5 * PAD + j] = bf16_hi(w.z);
+            dst[6 * PAD + j] = bf16_lo(w.w); dst[7 * PAD + j] = bf16_hi(w.w);
+        } else {
+            float *dst = &sv[tt][8 * (c - 2 * QC - AC)];
+            reinterpret_cast<float4 *>(dst)[0] =
+                make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+            reinterpret_cast<float4 *>(dst)[1] =
+                make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+        }
+    };
+    // extend: raw copies of the block starting at step tb into buffer buf, as one commit group
+    // (an empty group past the last block keeps the group count of every iteration the same)
+    auto issue_raw = [&](int buf, int tb) {
+        if (tb < steps) {
+            const int tn_b = steps - tb < TMAX ? steps - tb : TMAX;
+            for (int x = tid; x < tn_b * PER_TOK; x += NTHR) cp_async16(&raw[buf][x], item_src(x, tb));
+            if (tid < tn_b) cp_async4(&rawb[buf][tid], p.beta + token_row(tb + tid));
+        }
+        cp_async_commit();
+    };
+    if constexpr (BLOCKED) issue_raw(0, 0);  // in flight together with the state loads
 
     const int slot = p.state_idx ? p.state_idx[b] : b;
     float *Sb = p.S + ((size_t)slot * p.H + h) * (size_t)(DK * DV) + col0 + cg * 4;
@@ -160,91 +252,64 @@ __global__ void __launch_bounds__(kRowGroups *CW / 4, kda_min_blocks(CW, MODE))
     };
     if (state_first) pdl_wait_trigger();
 
-    // Only extend programs can exceed one block of TMAX tokens; for the others the loop body
-    // runs once with every step in it (and compiles to straight-line code).
-    constexpr bool BLOCKED = MODE == kExtend;
-    for (int t0 = 0; BLOCKED ? t0 < steps : t0 == 0; t0 += TMAX) {
+    // For the programs other than extend the loop body runs once with every step in it (and
+    // compiles to straight-line code).
+    for (int t0 = 0, blk = 0; BLOCKED ? t0 < steps : t0 == 0; t0 += TMAX, ++blk) {
         const int tn = !BLOCKED ? steps : (steps - t0 < TMAX ? steps - t0 : TMAX);
-        if (BLOCKED && t0 > 0) __syncthreads();  // the previous block's tokens are no longer read
 
-        // Token vectors of steps t0 .. t0+tn-1 into slots 0..tn-1.  Two loaders fill the same
+        // Token vectors of steps t0 .. t0+tn-1 into slots 0..tn-1.  The loaders fill the same
         // shared arrays with the same values (results do not depend on the choice); which is
-        // faster depends on the CTA width and the program length.  beta goes to a register
-        // first so its load overlaps the others.
+        // faster depends on the CTA width and the program length.
         float beta_r = 0.f;
-        if (tid < tn) {
-            const int t = t0 + tid;
-            beta_r = (t < n_pre ? p.betap : p.beta)[token_row(t)];
-        }
-        constexpr bool kVectorLoads = CW <= 32 || MODE == kReplayVerify || MODE == kExtend;
-        if constexpr (kVectorLoads) {
-            // per token DK/8 chunks of q, DK/8 of k, DK/4 of alpha and CW/8 of v, one 128-bit
-            // load each; a thread issues LDEPTH loads before storing any of them
-            constexpr int QC = DK / 8, AC = DK / 4, VC = CW / 8, PER_TOK = 2 * QC + AC + VC;
-            constexpr int LDEPTH = 4;
-            const int n_items = tn * PER_TOK;
-            for (int x0 = tid; x0 < n_items; x0 += LDEPTH * NTHR) {
-                uint4 r[LDEPTH];
+        if constexpr (BLOCKED) {
+            const int buf = blk & 1;
+            issue_raw(buf ^ 1, t0 + TMAX);  // the next block, into the buffer converted last time
+            cp_async_wait<1>();             // this thread's copies of this block have landed
+            __syncthreads();                // everyone's have; the previous block is no longer read
+            for (int x = tid; x < tn * PER_TOK; x += NTHR) store_item(x, raw[buf][x]);
+            if (tid < tn) beta_r = rawb[buf][tid];
+        } else {
+            // beta goes to a register first so its load overlaps the others
+            if (tid < tn) {
+                const int t = t0 + tid;
+                beta_r = (t < n_pre ? p.betap : p.beta)[token_row(t)];
+            }
+            constexpr bool kVectorLoads = CW <= 32 || MODE == kReplayVerify;
+            if constexpr (kVectorLoads) {
+                // one 128-bit load per item; a thread issues LDEPTH loads before storing any of them
+                constexpr int LDEPTH = 4;
+                const int n_items = tn * PER_TOK;
+                for (int x0 = tid; x0 < n_items; x0 += LDEPTH * NTHR) {
+                    uint4 r[LDEPTH];
 #pragma unroll
-                for (int u = 0; u < LDEPTH; ++u) {
-                    const int x = x0 + u * NTHR;
-                    if (x >= n_items) break;
-                    const int tt = x / PER_TOK, c = x - tt * PER_TOK;
+                    for (int u = 0; u < LDEPTH; ++u) {
+                        const int x = x0 + u * NTHR;
+                        if (x >= n_items) break;
+                        r[u] = ld_act_v4(item_src(x, t0));
+                    }
+#pragma unroll
+                    for (int u = 0; u < LDEPTH; ++u) {
+                        const int x = x0 + u * NTHR;
+                        if (x >= n_items) break;
+                        store_item(x, r[u]);
+                    }
+                }
+            } else {
+                // scalar loads, one unrolled pass per token (measured faster for 64/128-column
+                // slices in the decode, verify and replay programs)
+                for (int tt = 0; tt < tn; ++tt) {
                     const int t = t0 + tt;
                     const bool pre = t < n_pre;
+                    const uint16_t *q = pre ? p.qp : p.q, *k = pre ? p.kp : p.k, *v = pre ? p.vp : p.v;
+                    const float *al = pre ? p.alphap : p.alpha;
                     const size_t tok = token_row(t);
-                    const void *src;
-                    if (c < QC) src = (pre ? p.qp : p.q) + tok * DK + 8 * c;
-                    else if (c < 2 * QC) src = (pre ? p.kp : p.k) + tok * DK + 8 * (c - QC);
-                    else if (c < 2 * QC + AC) src = (pre ? p.alphap : p.alpha) + tok * DK + 4 * (c - 2 * QC);
-                    else src = (pre ? p.vp : p.v) + tok * DV + col0 + 8 * (c - 2 * QC - AC);
-                    r[u] = ld_act_v4(src);
-                }
-#pragma unroll
-                for (int u = 0; u < LDEPTH; ++u) {
-                    const int x = x0 + u * NTHR;
-                    if (x >= n_items) break;
-                    const int tt = x / PER_TOK, c = x - tt * PER_TOK;
-                    const uint4 w = r[u];
-                    if (c < 2 * QC + AC && c >= 2 * QC) {  // 4 alphas (fp32 bits), rows i0..i0+3
-                        const int i0 = 4 * (c - 2 * QC);
-                        sa[tt][rowpos(i0 + 0)] = __uint_as_float(w.x);
-                        sa[tt][rowpos(i0 + 1)] = __uint_as_float(w.y);
-                        sa[tt][rowpos(i0 + 2)] = __uint_as_float(w.z);
-                        sa[tt][rowpos(i0 + 3)] = __uint_as_float(w.w);
-                        continue;
+                    for (int i = tid; i < DK; i += NTHR) {
+                        sq[tt][rowpos(i)] = bf16_bits_to_float(q[tok * DK + i]);
+                        sk[tt][rowpos(i)] = bf16_bits_to_float(k[tok * DK + i]);
+                        sa[tt][rowpos(i)] = al[tok * DK + i];
                     }
-                    if (c < 2 * QC) {  // 8 bf16 of q or k, rows i0..i0+7 (one per row group)
-                        float *dst = c < QC ? sq[tt] : sk[tt];
-                        const int j = c < QC ? c : c - QC;  // i0 = 8 j: rows 8j .. 8j+7
-                        dst[0 * PAD + j] = bf16_lo(w.x); dst[1 * PAD + j] = bf16_hi(w.x);
-                        dst[2 * PAD + j] = bf16_lo(w.y); dst[3 * PAD + j] = bf16_hi(w.y);
-                        dst[4 * PAD + j] = bf16_lo(w.z); dst[5 * PAD + j] = bf16_hi(w.z);
-                        dst[6 * PAD + j] = bf16_lo(w.w); dst[7 * PAD + j] = bf16_hi(w.w);
-                        continue;
-                    }
-                    float *dst = &sv[tt][8 * (c - 2 * QC - AC)];
-                    reinterpret_cast<float4 *>(dst)[0] =
-                        make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
-                    reinterpret_cast<float4 *>(dst)[1] =
-                        make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+                    for (int c = tid; c < CW; c += NTHR) sv[tt][c] = bf16_bits_to_float(v[tok * DV + col0 + c]);
                 }
-            }
-        } else {
-            // scalar loads, one unrolled pass per token (measured faster for 64/128-column
-            // slices in the decode, verify and replay programs)
-            for (int tt = 0; tt < tn; ++tt) {
-                const int t = t0 + tt;
-                const bool pre = t < n_pre;
-                const uint16_t *q = pre ? p.qp : p.q, *k = pre ? p.kp : p.k, *v = pre ? p.vp : p.v;
-                const float *al = pre ? p.alphap : p.alpha;
-                const size_t tok = token_row(t);
-                for (int i = tid; i < DK; i += NTHR) {
-                    sq[tt][rowpos(i)] = bf16_bits_to_float(q[tok * DK + i]);
-                    sk[tt][rowpos(i)] = bf16_bits_to_float(k[tok * DK + i]);
-                    sa[tt][rowpos(i)] = al[tok * DK + i];
-                }
-                for (int c = tid; c < CW; c += NTHR) sv[tt][c] = bf16_bits_to_float(v[tok * DV + col0 + c]);
             }
         }
         if (tid < tn) sb[tid] = beta_r;
@@ -353,8 +418,8 @@ int launch_dk(int cw, const KdaParams &p, cudaStream_t st) {
 //           heads do not cover the SMs twice (batch 16 separate window: 23.1 us vs 26.7 with
 //           32 and 32.2 with 16; batch 64: 81.5 vs 96.3 and 132);
 //   extend: whole heads (128 columns) while the heads fit one per SM, so each serial chain
-//           has an SM to itself (4 x 512-token chunks: 391 us vs 484 with 64 and 580 with 32),
-//           else 64 (60 decodes + 4 x 128-token chunks: 184 us vs 201 with 128).
+//           has an SM to itself (4 x 512-token chunks: 314 us vs 349 with 64), else 64 (60
+//           decodes + 4 x 128-token chunks: 128.6 us vs 141 with 128).
 int choose_cw(int B, int H, int dv, int mode) {
     const char *env = getenv("HLA_KDA_CW");
     if (env) {

@@ -249,10 +249,13 @@ def test_extend_single_tokens_equal_decode_bitwise(dev):
     assert torch.equal(S1, S2) and torch.equal(o1, o2)
 
 
-@pytest.mark.parametrize("lens,d", [([0, 1, 5, 17, 3, 40, 8, 1], 128), ([2, 0, 9], 64)])
+@pytest.mark.parametrize("lens,d", [([0, 1, 5, 17, 3, 40, 8, 1], 128), ([2, 0, 9], 64),
+                                    ([int(n) for n in np.random.default_rng(5).choice([0, 1, 1, 1, 2, 9, 20], 300)], 64)])
 def test_extend_ragged_mixed_batch(dev, lens, d):
     """Ragged sequences (empty, single-token decode, multi-block prefill chunks) in one call:
-    against the oracle, and bitwise against one decode call per token."""
+    against the oracle, and bitwise against one decode call per token.  The kernel schedules the
+    multi-block chains first; 300 sequences take the schedule through several rounds of its
+    block-wide count (128 threads per CTA)."""
     B = len(lens)
     H = 32 if d == 128 else 4
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
