@@ -400,9 +400,10 @@ def extend_sweep(torch, hla, inputs, dev, peak):
 def spec_sweep(torch, hla, inputs, wl, dev, peak):
     """Speculative window, T=4, accepted length uniform in 0..4, at B=16 and B=64, two forms per
     step: separate (verify + accept + replay) and fused (replay of the previous window with the
-    verify of the next + accept).  Each step takes the next B committed states of a 768 MB pool
-    (> 3x L2) through state_idx, so every step reads its states from HBM; the inputs rotate
-    through 4 windows.  tokens/s counts accepted tokens."""
+    verify of the next + accept); and the verify and replay programs each alone.  Each step takes
+    the next B committed states of a 768 MB pool (> 3x L2) through state_idx, so every step reads
+    its states from HBM; the inputs rotate through 4 windows.  tokens/s counts accepted tokens
+    (verify alone: the drafted tokens it scores)."""
     c = CFG
     T, H, d = SWEEP_T, c["H"], c["d"]
     tok = 3 * d * 2 + d * 4 + 4
@@ -445,15 +446,31 @@ def spec_sweep(torch, hla, inputs, wl, dev, peak):
                                            p_["alpha"], p_["beta"], acc, w["q"], w["k"], w["v"],
                                            w["alpha"], w["beta"], o)
                 hla.spec_accept_prefix(B, T, dr, tg, acc, com)
+        accs = [torch.from_numpy(ids[r][2].astype("int32")).to(dev) for r in range(ROTATE)]
+
+        def verify_only(i, B=B, wins=wins, o=o, idxs=idxs):
+            w = wins[i % ROTATE]
+            hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, pool, idxs[i], w["q"], w["k"],
+                                       w["v"], w["alpha"], w["beta"], None, o)
+
+        def replay_only(i, B=B, wins=wins, accs=accs, idxs=idxs):
+            w = wins[i % ROTATE]
+            hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, pool, idxs[i], w["q"], w["k"],
+                                       w["v"], w["alpha"], w["beta"], accs[i % ROTATE], None)
         mean_sep = statistics.mean(sum(spec_bytes(B, T, ids[r][2]).values()) for r in range(ROTATE))
+        mean_ver = statistics.mean(spec_bytes(B, T, ids[r][2])["verify"] for r in range(ROTATE))
+        mean_rep = statistics.mean(spec_bytes(B, T, ids[r][2])["replay"] for r in range(ROTATE))
         mean_fused = statistics.mean(
             B * H * 4 * d * d + sum(H * (4 * d * d + int(a) * tok) for a in ids[r][2] if a > 0)
             + B * H * T * (tok + 4 * d) + 2 * B * T * 4 + 3 * B * 4 for r in range(ROTATE))
         accepted = statistics.mean(float(sum(ids[r][2])) for r in range(ROTATE))
-        for name, fn, nbytes in (("separate", separate, mean_sep), ("fused", fused, mean_fused)):
+        for name, fn, nbytes, ntok in (("separate", separate, mean_sep, accepted),
+                                       ("fused", fused, mean_fused, accepted),
+                                       ("verify alone", verify_only, mean_ver, float(B * T)),
+                                       ("replay alone", replay_only, mean_rep, accepted)):
             t = graph_time(torch, fn, iters)
             res.append(dict(batch=B, form=name, us=round(t * 1e6, 2), bytes=round(nbytes),
-                            accepted_tokens=accepted, tokens_per_s=round(accepted / t),
+                            accepted_tokens=accepted, tokens_per_s=round(ntok / t),
                             gbs=round(nbytes / t / 1e9, 1), frac=round(nbytes / t / 1e9 / peak, 3)))
     del pool
     return res
