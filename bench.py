@@ -828,6 +828,25 @@ def run_profile(kind, iters=3):
         info.update(B=B, T=T, accepted=a.tolist(), verify_bytes=spec_bytes(B, T, a.cpu().numpy())["verify"],
                     replay_bytes=spec_bytes(B, T, a.cpu().numpy())["replay"],
                     variant=[verify_variant, hla.hla_last_variant()])
+    elif kind == "fused":
+        # the fused speculative step at batch 64: the previous window's accepted prefix replayed and
+        # committed, then this window verified, in one pass over the state (134 MB, > L2)
+        B, T, H, d = 64, c["spec_T"], c["H"], c["d"]
+        S = torch.randn(B, H, d, d, device=dev).mul_(0.05)
+        prev = inputs.kda_inputs((B, T), H, d, d, g, dev)
+        w = inputs.kda_inputs((B, T), H, d, d, g, dev)
+        _, _, a = inputs.accept_ids(B, T, g, dev)
+        acc = a.to(torch.int32)
+        o = torch.empty(B, T, H, d, device=dev)
+        for _ in range(iters):
+            hla.kda_spec_replay_verify(B, T, T, H, d, d, S, None, prev["q"], prev["k"], prev["v"],
+                                       prev["alpha"], prev["beta"], acc, w["q"], w["k"], w["v"],
+                                       w["alpha"], w["beta"], o)
+        an = a.cpu().numpy()
+        tok = 3 * d * 2 + d * 4 + 4
+        nbytes = (B * H * 4 * d * d + sum(H * (4 * d * d + int(x) * tok) for x in an if x > 0)
+                  + B * H * T * (tok + 4 * d))
+        info.update(B=B, T=T, accepted=an.tolist(), bytes=int(nbytes), variant=hla.hla_last_variant())
     elif kind == "extend":
         # four 512-token prefill chunks through kda_extend: each (sequence, head) is one serial
         # chain of 512 steps (8 MB of state; the kernel is bound by its step latency, not HBM)
@@ -1098,7 +1117,8 @@ def main():
     ap.add_argument("--threads", type=int, default=0,
                     help="reference arm: host threads the oracle may use (0 = every core); the "
                          "BLAS thread count is fixed by its environment variables at start-up")
-    ap.add_argument("--profile", choices=["moe", "kda", "spec", "extend", "dense", "dense16", "layer1", "layer8"],
+    ap.add_argument("--profile", choices=["moe", "kda", "spec", "fused", "extend", "dense", "dense16", "layer1",
+                                          "layer8"],
                     help="run one small case of a hot kernel (for ncu captures) and exit")
     ap.add_argument("--prefetch-ab", action="store_true",
                     help="time the layer under every side-stream prefetch mask and exit")
