@@ -67,6 +67,16 @@ PdlChain::~PdlChain() {
     g_pdl_started = prev_started || (same_stream && launched_inside);
 }
 
+// Entry points that launch several kernels chain them up to 32 tokens.  Measured on the decode layer
+// (CUDA graph of 8 calls with the prefetch stream, same box, medians of 5 interleaved repetitions,
+// plain / chained): batch 1 198.3 / 194.2 us, 2 297.6 / 293.5, 8 812.6 / 809.5, 32 2094.5 / 2086.5,
+// 64 2860.7 / 2871.0.  HLA_PDL=0 / 1 forces plain launches / chains.
+bool pdl_default(int M) {
+    const char *env = getenv("HLA_PDL");
+    if (env) return env[0] == '1';
+    return M <= 32;
+}
+
 bool pdl_for(cudaStream_t st) { return g_pdl_on && g_pdl_started && st == g_pdl_stream; }
 
 // records that a kernel went out on the chain's stream (chained or not)

@@ -74,6 +74,7 @@ struct PdlChain {
     bool prev_on, prev_started;
     cudaStream_t prev_st;
 };
+bool pdl_default(int M);             // do multi-kernel entry points chain their kernels at M tokens?
 bool pdl_for(cudaStream_t st);       // launch with programmatic serialisation on this stream?
 void pdl_launched(cudaStream_t st);  // a kernel was launched on st (the chain has started)
 

@@ -686,6 +686,7 @@ extern "C" int skinny_proj_splitk(int M, int N, int K, const hla_bf16 *x, const 
     cudaStream_t st = (cudaStream_t)stream;
     set_variant("skinny_proj<tt%d,%ssplit%d>", dense_tokens_per_tile(M),
                 !dense_tc_enabled(M) && dense_xi_applies(N, K, s) ? "xi," : "", s);
+    const PdlChain chain(st, pdl_default(M));  // the projection and its split reduction
     if (s == 1) return run_dense(M, N, K, x, W, 1, nullptr, y, y_dtype == HLA_BF16, residual, st);
     int r = run_dense(M, N, K, x, W, s, reinterpret_cast<float *>(ws), nullptr, 0, nullptr, st);
     if (r != HLA_OK) return r;
@@ -713,6 +714,7 @@ extern "C" int kda_qkvg_proj(int M, int Hd, int H, int dk, int dv, const hla_bf1
     HLA_REQUIRE(aligned16(ws), HLA_ERR_MISALIGNED);
     const int s = resolve_split(M, 4 * H * dk + H, Hd, split);
     set_variant("qkvg_proj<tt%d,split%d>", dense_tokens_per_tile(M), s);
+    const PdlChain chain((cudaStream_t)stream, pdl_default(M));  // the projection and its epilogue
     return run_qkvg(M, Hd, H, dk, x, W, q, k, v, alpha, beta, s, reinterpret_cast<float *>(ws),
                     (cudaStream_t)stream);
 }
@@ -745,6 +747,7 @@ extern "C" int moe_route_topk(int M, int Hd, int E, int k, const hla_bf16 *x, co
     HLA_REQUIRE(ws && ws_bytes >= need, HLA_ERR_WORKSPACE);
     HLA_REQUIRE(aligned16(ws), HLA_ERR_MISALIGNED);
     set_variant("router<split%d>", router_split(M, Hd, E));
+    const PdlChain chain((cudaStream_t)stream, pdl_default(M));  // the router GEMV and its top-k
     return run_router(M, Hd, E, k, x, W_r, topk_idx, topk_w, logits, reinterpret_cast<float *>(ws),
                       (cudaStream_t)stream);
 }
@@ -787,6 +790,7 @@ extern "C" int skinny_proj_residual_rmsnorm(int M, int N, int K, const hla_bf16 
     const int s = residual_norm_split(M, N, K, split);
     cudaStream_t st = (cudaStream_t)stream;
     float *part = reinterpret_cast<float *>(ws);
+    const PdlChain chain(st, pdl_default(M));  // the projection and its residual + RMSNorm epilogue
     int rc = run_dense(M, N, K, x, W, s, part, nullptr, 0, nullptr, st);
     if (rc != HLA_OK) return rc;
     const cudaError_t e = launch_kernel(

@@ -81,16 +81,6 @@ ForkJoin *fork_join_events() {
     return &e;
 }
 
-// Whether the layer's kernels form a programmatic-launch chain (HLA_PDL=0/1 overrides).
-// Measured (CUDA graph of 8 layers with the prefetch stream, same box, medians of 5 interleaved
-// repetitions, plain / chained): batch 1 198.3 / 194.2 us, 2 297.6 / 293.5, 8 812.6 / 809.5,
-// 32 2094.5 / 2086.5, 64 2860.7 / 2871.0.  Chained up to 32 tokens.
-bool layer_pdl(int M) {
-    const char *env = getenv("HLA_PDL");
-    if (env) return env[0] == '1';
-    return M <= 32;
-}
-
 }  // namespace
 
 bool moe_shared_on_side(int M, int nsh, bool have_side);
@@ -135,7 +125,7 @@ extern "C" int hla_decode_layer(const hla_layer *L, int M, const hla_bf16 *x, fl
     // it loads its static weights or its state while its predecessor finishes.  The first is a
     // plain launch after whatever the caller queued (or, inside a chain the caller opened, the
     // next link of that chain).  Side-stream launches stay plain.
-    const PdlChain chain(st, layer_pdl(M));
+    const PdlChain chain(st, pdl_default(M));
     if ((r = hla_rmsnorm(M, Hd, x, L->gamma_attn, L->eps, bf(lo.x1), stream)) != HLA_OK) return r;
     if ((r = kda_qkvg_proj(M, Hd, H, d, d, bf(lo.x1), L->W_qkvgb, bf(lo.q), bf(lo.k), bf(lo.v),
                            f32(lo.alpha), f32(lo.beta), 0, w + lo.qkvg_ws, lo.qkvg_bytes,
@@ -180,7 +170,7 @@ extern "C" int hla_decode_layer(const hla_layer *L, int M, const hla_bf16 *x, fl
                                  w + lo.moe_ws, lo.moe_bytes, st, pf, shared_side)) != HLA_OK)
         return r;
     if (layer_pf && cudaStreamWaitEvent(st, ev->join, 0) != cudaSuccess) return HLA_ERR_CUDA;
-    set_variant("decode_layer%s%s", pf ? "<prefetch>" : "", layer_pdl(M) ? "<pdl>" : "");
+    set_variant("decode_layer%s%s", pf ? "<prefetch>" : "", pdl_default(M) ? "<pdl>" : "");
     return HLA_OK;
 }
 

@@ -1024,6 +1024,7 @@ int moe_forward_checked(int M, int Hd, int I, int E, int k, int n_shared, const 
     const size_t need = moe_workspace_bytes(M, Hd, I, E, k, n_shared);
     HLA_REQUIRE(ws && ws_bytes >= need, HLA_ERR_WORKSPACE);
     HLA_REQUIRE(aligned16(ws), HLA_ERR_MISALIGNED);
+    const PdlChain chain(st, pdl_default(M));  // dispatch, experts and combine as one chain
     return run_moe(M, Hd, I, E, k, n_shared, x, topk_idx, topk_w, W_gate, W_up, W_down, Ws_gate,
                    Ws_up, Ws_down, residual, y, ws, st, pf, shared_external);
 }

@@ -60,6 +60,7 @@ extern "C" int skinny_proj_splitk_noalloc(int M, int N, int K, const hla_bf16 *x
     // same variant text as skinny_proj_splitk after the prefix (which streaming kernel, which split)
     set_variant("skinny_proj_noalloc<tt%d,%ssplit%d>", dense_tokens_per_tile(M),
                 !dense_tc_enabled(M) && dense_xi_applies(N, K, s) ? "xi," : "", s);
+    const PdlChain chain(st, pdl_default(M));  // the projection and its split reduction
     if (s == 1) return run_dense(M, N, K, x, W, 1, nullptr, y, y_dtype == HLA_BF16, residual, st);
     float *scratch = nullptr;
     int r = scratch_for_current_device(&scratch);

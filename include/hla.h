@@ -106,8 +106,11 @@ int hla_version(void);
  * norm gains of its own call: inside a chain these must not be written by the call right before
  * it (weights are static in the decode loop).  Side streams are not part of the chain.  One chain
  * per host thread: a second hla_chain_begin, or hla_chain_end without one, returns
- * HLA_ERR_INVALID_ARG.  hla_decode_layer chains its own kernels at up to 32 tokens and, inside a
- * caller's chain on the same stream, continues it.
+ * HLA_ERR_INVALID_ARG.  Every entry point that launches several kernels (hla_decode_layer,
+ * kda_qkvg_proj, skinny_proj_splitk and its no-allocation form, skinny_proj_residual_rmsnorm,
+ * moe_route_topk, moe_expert_forward) chains its own kernels at up to 32 tokens (the environment
+ * variable HLA_PDL=0 / 1 turns that off / on at any size) and, inside a caller's chain on the same
+ * stream, continues it.  Its first kernel follows whatever the caller queued before it.
  * -------------------------------------------------------------------------*/
 int hla_chain_begin(hla_stream stream);
 int hla_chain_end(void);

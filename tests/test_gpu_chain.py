@@ -118,3 +118,60 @@ def test_chain_of_calls_on_the_same_state(dev):
         S_c, o_c = run(True)
         assert torch.equal(S_c, S_ref)
         assert all(torch.equal(a, b) for a, b in zip(o_c, o_ref))
+
+
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_entry_points_chain_their_own_kernels_bitwise(dev, M, monkeypatch):
+    """The multi-kernel entry points (projections with their epilogues or split reductions, the
+    router, the expert pipeline) chain their own kernels up to 32 tokens; HLA_PDL=0 launches them
+    plain.  Both give the same bits, with the expert weights' shapes of the model at a reduced
+    expert count."""
+    Hd, I, E, k, ns, H, d = 7168, 2048, 24, 8, 1, 32, 128
+    g = inputs.generator(5100 + M, dev)
+    w = inputs.moe_weights(E, Hd, I, ns, g, device=dev)
+    Wq = inputs.weight((4 * H * d + H, Hd), g, dev)
+    Wo = inputs.weight((Hd, H * d), g, dev)
+    gamma = inputs.gains(Hd, g, dev)
+    x = inputs.activations(M, Hd, g, dev)
+    o_in = inputs.activations(M, H * d, g, dev)
+    res = inputs.activations(M, Hd, g, dev)
+
+    def ws(n):
+        return torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+
+    def run():
+        out = {}
+        q, kk_, v = (torch.empty(M, H, d, dtype=torch.bfloat16, device=dev) for _ in range(3))
+        al, be = torch.empty(M, H, d, device=dev), torch.empty(M, H, device=dev)
+        nb = hla.kda_qkvg_proj_workspace_size(M, Hd, H, d, d, 0)
+        hla.kda_qkvg_proj(M, Hd, H, d, d, x, Wq, q, kk_, v, al, be, 0, ws(nb), nb)
+        out.update(q=q, k=kk_, v=v, alpha=al, beta=be)
+        y = torch.empty(M, Hd, device=dev)
+        nb = hla.skinny_proj_splitk_workspace_size(M, Hd, H * d, 4)
+        hla.skinny_proj_splitk(M, Hd, H * d, o_in, Wo, res, y, hla.HLA_F32, 4, ws(nb), nb)
+        out["proj"] = y
+        r = torch.empty(M, Hd, dtype=torch.bfloat16, device=dev)
+        xn = torch.empty(M, Hd, dtype=torch.bfloat16, device=dev)
+        nb = hla.skinny_proj_residual_rmsnorm_workspace_size(M, Hd, H * d, 0)
+        hla.skinny_proj_residual_rmsnorm(M, Hd, H * d, o_in, Wo, res, gamma, 1e-6, r, xn, 0, ws(nb), nb)
+        out.update(r=r, xn=xn)
+        idx = torch.empty(M, k, dtype=torch.int32, device=dev)
+        wt = torch.empty(M, k, device=dev)
+        nb = hla.moe_route_topk_workspace_size(M, Hd, E)
+        hla.moe_route_topk(M, Hd, E, k, xn, w["W_r"], idx, wt, None, ws(nb), nb)
+        out.update(idx=idx, wt=wt)
+        ym = torch.empty(M, Hd, dtype=torch.bfloat16, device=dev)
+        nb = hla.moe_expert_forward_workspace_size(M, Hd, I, E, k, ns)
+        hla.moe_expert_forward(M, Hd, I, E, k, ns, xn, idx, wt, w["W_gate"], w["W_up"], w["W_down"],
+                               w["Ws_gate"], w["Ws_up"], w["Ws_down"], r, ym, ws(nb), nb)
+        out["moe"] = ym
+        torch.cuda.synchronize()
+        return {kk: vv.cpu() for kk, vv in out.items()}
+
+    monkeypatch.setenv("HLA_PDL", "0")
+    plain = run()
+    monkeypatch.setenv("HLA_PDL", "1")
+    chained = run()
+    assert hla.hla_device_status() == 0
+    for key in plain:
+        assert torch.equal(plain[key], chained[key]), key
