@@ -147,6 +147,37 @@ def test_spec_window_config(dev):
             assert torch.equal(Sg[b], S0[b])
 
 
+@pytest.mark.parametrize("T,d,o_bf16", [(1, 128, False), (3, 64, True), (7, 128, True), (8, 64, False)])
+def test_spec_window_draft_lengths(dev, T, d, o_bf16):
+    """Verify and replay at other draft lengths and head sizes, states in a slot pool, against the
+    oracle's sequential steps."""
+    B, H = 5, 8
+    S0 = warm_states(11, B, H, d)
+    g = inputs.generator(1100 + T + d)
+    win = inputs.kda_inputs((B, T), H, d, d, g)
+    draft, target, a = inputs.accept_ids(B, T, g)
+    perm = torch.randperm(B + 2, generator=inputs.generator(1101))[:B].to(torch.int32)
+    pool = torch.zeros(B + 2, H, d, d)
+    pool[perm.long()] = S0
+    S = pool.to(dev)
+    wd, wn = _to(win, dev), _np(win)
+    o = torch.empty(B, T, H, d, device=dev, dtype=torch.bfloat16 if o_bf16 else torch.float32)
+    hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, S, perm.to(dev), wd["q"], wd["k"], wd["v"],
+                               wd["alpha"], wd["beta"], None, o, hla.HLA_BF16 if o_bf16 else hla.HLA_F32)
+    acc = torch.zeros(B, dtype=torch.int32, device=dev)
+    com = torch.zeros(B, dtype=torch.int32, device=dev)
+    hla.spec_accept_prefix(B, T, draft.to(dev), target.to(dev), acc, com)
+    hla.kda_spec_verify_replay(hla.HLA_SPEC_REPLAY, B, T, H, d, d, S, perm.to(dev), wd["q"], wd["k"], wd["v"],
+                               wd["alpha"], wd["beta"], acc, None)
+    torch.cuda.synchronize()
+    assert np.array_equal(acc.cpu().numpy(), a.numpy())
+    o_ref = oracle.kda.spec_verify(f64(S0), wn["q"], wn["k"], wn["v"], wn["alpha"], wn["beta"])
+    S_ref = oracle.kda.spec_replay(f64(S0), wn["q"], wn["k"], wn["v"], wn["alpha"], wn["beta"], a.numpy())
+    # bf16 output: rounding of 2^-9 relative on top of the fp32 path
+    assert max_rel(f64(o), o_ref) < (5e-3 if o_bf16 else KDA_MAX_REL)
+    assert max_rel(S.cpu()[perm.long()].double().numpy(), S_ref) < KDA_MAX_REL
+
+
 def test_replay_all_equals_decode_steps_bitwise(dev):
     B, T, H, d = 4, 4, 32, 128
     S0 = warm_states(3, B, H, d)

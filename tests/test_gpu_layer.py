@@ -174,3 +174,30 @@ def test_layer_programmatic_launch_is_bitwise_neutral(dev, layer, M, monkeypatch
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(y, out["0"][0]) and torch.equal(S_graph, out["0"][1])
+
+
+@pytest.mark.parametrize("M", [1, 8, 64])
+def test_layer_state_pool_matches_identity(dev, layer, M):
+    """The layer with its states in a larger slot pool (state_idx: a seeded permutation) gives the
+    bits of the layer on the same states stored in order, and leaves every other slot untouched."""
+    w, L, p = layer
+    x = inputs.activations(M, FULL["Hd"], inputs.generator(4800 + M)).to(dev)
+    S0 = warm_states(6, M, H, D)
+    ref_S = S0.to(dev)
+    ref_y = _run(dev, L, M, x, ref_S)
+    P = M + 5
+    perm = torch.randperm(P, generator=inputs.generator(4801 + M))[:M].to(torch.int32)
+    pool0 = torch.randn(P, H, D, D, generator=inputs.generator(4802 + M)).mul_(0.05)
+    pool0[perm.long()] = S0
+    pool = pool0.to(dev)
+    y = torch.empty(M, FULL["Hd"], dtype=torch.bfloat16, device=dev)
+    nb = hla.hla_decode_layer_workspace_size(L, M)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    hla.hla_decode_layer(L, M, x, pool, perm.to(dev), y, ws, nb, prefetch_stream=0)
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref_y)
+    got = pool.cpu()
+    assert torch.equal(got[perm.long()], ref_S.cpu())
+    others = torch.ones(P, dtype=torch.bool)
+    others[perm.long()] = False
+    assert torch.equal(got[others], pool0[others])
