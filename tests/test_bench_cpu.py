@@ -20,9 +20,9 @@ def test_reference_arm_prints_one_contract_line():
     lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
     assert len(lines) == 1
     d = json.loads(lines[0])
-    with open(os.path.join(ROOT, "BASELINE.json")) as f:
-        metric = json.load(f)["metric"]
-    assert d["impl"] == "reference" and d["metric"] == metric
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC  # the GPU arm's metric
     assert d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["value"] > 0 and d["ms_per_step"] > 0
