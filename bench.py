@@ -330,7 +330,8 @@ def kda_sweep(torch, hla, inputs, dev, peak):
 
 
 def moe_sweep(torch, hla, inputs, wl, dev, peak):
-    """Router + experts alone at M in {1,2,8,32,64} (the weights are ~22.5 GB: always cold)."""
+    """Router + experts alone at M in {1,2,8,32,64} (the weights are ~22.5 GB: always cold), the two
+    calls bracketed as one launch chain (HLA_BENCH_CHAIN=0: plain)."""
     c = CFG
     res = []
     for M in (1, 2, 8, 32, 64):
@@ -351,10 +352,11 @@ def moe_sweep(torch, hla, inputs, wl, dev, peak):
 
         def fn(i):
             x = xs[i % ROTATE]
-            hla.moe_route_topk(M, c["Hd"], c["E"], c["k"], x, w["W_r"], idx, wt, None, rws, rb)
-            hla.moe_expert_forward(M, c["Hd"], c["I"], c["E"], c["k"], c["n_shared"], x, idx, wt,
-                                   w["W_gate"], w["W_up"], w["W_down"], w["Ws_gate"], w["Ws_up"],
-                                   w["Ws_down"], None, y, mws, nb)
+            with launch_chain(hla):  # the router's top-k and the dispatch as one chain, as in the layer
+                hla.moe_route_topk(M, c["Hd"], c["E"], c["k"], x, w["W_r"], idx, wt, None, rws, rb)
+                hla.moe_expert_forward(M, c["Hd"], c["I"], c["E"], c["k"], c["n_shared"], x, idx, wt,
+                                       w["W_gate"], w["W_up"], w["W_down"], w["Ws_gate"], w["Ws_up"],
+                                       w["Ws_down"], None, y, mws, nb)
         t = graph_time(torch, fn, 4 * ROTATE)
         U = statistics.mean(us)
         nbytes = layer_bytes(M, U)["router"] + layer_bytes(M, U)["experts"]
