@@ -92,6 +92,29 @@ def test_decode_step_sweep(dev, B):
     assert hla.hla_last_variant().startswith("kda_recur<dk128")
 
 
+@pytest.mark.parametrize("B,cw", [(1, "0"), (8, "0"), (64, "0"), (8, "32"), (8, "64")])
+def test_decode_step_d64(dev, B, cw, monkeypatch):
+    """d_k = d_v = 64 (the other supported head size) against the oracle, at the default slice
+    width and forced wider ones (whole heads at 64), with bits equal across widths."""
+    H, d = 16, 64
+    monkeypatch.setenv("HLA_KDA_CW", cw)
+    S0 = warm_states(3, B, H, d)
+    inp = inputs.kda_inputs((B,), H, d, d, inputs.generator(1200 + B))
+    S = S0.to(dev)
+    o = _decode(dev, S, _to(inp, dev))
+    torch.cuda.synchronize()
+    assert hla.hla_last_variant().startswith("kda_recur<dk64")
+    n = _np(inp)
+    S_ref, o_ref = oracle.kda.kda_step(f64(S0), n["q"], n["k"], n["v"], n["alpha"], n["beta"])
+    assert max_rel(f64(o), o_ref) < KDA_MAX_REL
+    assert max_rel(f64(S), S_ref) < KDA_MAX_REL
+    monkeypatch.setenv("HLA_KDA_CW", "16")
+    S16 = S0.to(dev)
+    o16 = _decode(dev, S16, _to(inp, dev))
+    torch.cuda.synchronize()
+    assert torch.equal(S16, S) and torch.equal(o16, o)
+
+
 def test_decode_bf16_output_and_state_idx(dev):
     B, H, d = 8, 32, 128
     S0 = warm_states(1, B, H, d)
@@ -264,6 +287,26 @@ def test_fused_replay_verify(dev, B, Tp, T, d, acc_kind):
     for b in range(B):
         if int(acc[b]) == 0:
             assert torch.equal(S1[b].cpu(), S0[b])
+
+
+def test_extend_bf16_output_is_the_rounded_fp32_output(dev):
+    """kda_extend with bf16 outputs: the same fp32 arithmetic, rounded to nearest even at the store,
+    so each output equals the fp32 run's output rounded to bf16; the states are bitwise equal."""
+    lens = [3, 1, 20, 0, 9]
+    B, H, d = len(lens), 8, 128
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32), device=dev)
+    N = int(sum(lens))
+    S0 = warm_states(12, B, H, d)
+    tok = _to(inputs.kda_inputs((N,), H, d, d, inputs.generator(1300)), dev)
+    out = {}
+    for dt, tdt in ((hla.HLA_F32, torch.float32), (hla.HLA_BF16, torch.bfloat16)):
+        S = S0.to(dev)
+        o = torch.empty(N, H, d, device=dev, dtype=tdt)
+        hla.kda_extend(B, cu, H, d, d, S, None, tok["q"], tok["k"], tok["v"], tok["alpha"], tok["beta"], o, dt)
+        torch.cuda.synchronize()
+        out[dt] = (S, o)
+    assert torch.equal(out[hla.HLA_F32][0], out[hla.HLA_BF16][0])
+    assert torch.equal(out[hla.HLA_F32][1].to(torch.bfloat16), out[hla.HLA_BF16][1])
 
 
 def test_extend_single_tokens_equal_decode_bitwise(dev):
