@@ -39,8 +39,9 @@
  *  - A failed launch returns HLA_ERR_CUDA (cudaGetLastError is consumed).
  *  - Entry points keep no state between calls apart from: the device status word
  *    (hla_device_status), the calling thread's last-variant string, the
- *    instrumentation counters, per-device cached attributes and per-thread events
- *    of the side-stream fork/join, and the one scratch array shared by every
+ *    instrumentation counters, per-device cached attributes, per-thread and per-device events
+ *    of the side-stream fork/join, the calling thread's open launch chain
+ *    (hla_chain_begin), and the one scratch array shared by every
  *    skinny_proj_splitk_noalloc call.  Calls on different streams may run
  *    concurrently when their buffers do not overlap (skinny_proj_splitk_noalloc
  *    excepted: see there).
