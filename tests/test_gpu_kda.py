@@ -201,6 +201,37 @@ def test_spec_window_draft_lengths(dev, T, d, o_bf16):
     assert max_rel(S.cpu()[perm.long()].double().numpy(), S_ref) < KDA_MAX_REL
 
 
+def test_verify_with_vanishing_decays(dev):
+    """Verify where some rows' decays vanish (exact zeros, and tiny values whose products underflow)
+    next to ordinary ones, against the oracle; a fused replay-and-verify of the same window (nothing
+    replayed) gives the same bits as the separate call."""
+    B, T, H, d = 4, 4, 8, 128
+    S0 = warm_states(13, B, H, d)
+    g = inputs.generator(1400)
+    win = inputs.kda_inputs((B, T), H, d, d, g)
+    al = win["alpha"]
+    al[0, 1, 2, 5] = 0.0          # one row of one head of sequence 0 forgets everything at token 1
+    al[1, :, 3, 7:9] = 1e-30      # two rows of a head of sequence 1 underflow over the window
+    al[2, 0, :, 64] = 1e-12       # one row of every head of sequence 2 (products reach 1e-48)
+    wd, wn = _to(win, dev), _np(win)
+    S = S0.to(dev)
+    o = torch.empty(B, T, H, d, device=dev)
+    hla.kda_spec_verify_replay(hla.HLA_SPEC_VERIFY, B, T, H, d, d, S, None, wd["q"], wd["k"], wd["v"],
+                               wd["alpha"], wd["beta"], None, o)
+    torch.cuda.synchronize()
+    o_ref = oracle.kda.spec_verify(f64(S0), wn["q"], wn["k"], wn["v"], wn["alpha"], wn["beta"])
+    assert torch.isfinite(o).all()
+    assert max_rel(f64(o), o_ref) < KDA_MAX_REL
+    # fused: replay nothing of a previous window (accepted 0), then verify this one
+    acc0 = torch.zeros(B, dtype=torch.int32, device=dev)
+    o2 = torch.empty_like(o)
+    S2 = S0.to(dev)
+    hla.kda_spec_replay_verify(B, T, T, H, d, d, S2, None, wd["q"], wd["k"], wd["v"], wd["alpha"], wd["beta"],
+                               acc0, wd["q"], wd["k"], wd["v"], wd["alpha"], wd["beta"], o2)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o) and torch.equal(S2, S)
+
+
 def test_replay_all_equals_decode_steps_bitwise(dev):
     B, T, H, d = 4, 4, 32, 128
     S0 = warm_states(3, B, H, d)
