@@ -170,11 +170,11 @@ def test_spec_window_config(dev):
             assert torch.equal(Sg[b], S0[b])
 
 
-@pytest.mark.parametrize("T,d,o_bf16", [(1, 128, False), (3, 64, True), (7, 128, True), (8, 64, False)])
-def test_spec_window_draft_lengths(dev, T, d, o_bf16):
-    """Verify and replay at other draft lengths and head sizes, states in a slot pool, against the
-    oracle's sequential steps."""
-    B, H = 5, 8
+@pytest.mark.parametrize("B,H,T,d,o_bf16", [(5, 8, 1, 128, False), (5, 8, 3, 64, True), (5, 8, 7, 128, True),
+                                            (5, 8, 8, 64, False), (64, 32, 4, 128, False)])
+def test_spec_window_draft_lengths(dev, B, H, T, d, o_bf16):
+    """Verify and replay at other draft lengths, head sizes and batch 64 (the sweep's larger window),
+    states in a slot pool, against the oracle's sequential steps."""
     S0 = warm_states(11, B, H, d)
     g = inputs.generator(1100 + T + d)
     win = inputs.kda_inputs((B, T), H, d, d, g)
