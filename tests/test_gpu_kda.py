@@ -280,7 +280,8 @@ def test_run_to_run_determinism(dev):
 
 
 @pytest.mark.parametrize("B,Tp,T,d,acc_kind", [(16, 4, 4, 128, "uniform"), (4, 3, 5, 128, "zero"),
-                                                (4, 8, 8, 128, "all"), (2, 4, 2, 64, "uniform")])
+                                                (4, 8, 8, 128, "all"), (2, 4, 2, 64, "uniform"),
+                                                (64, 4, 4, 128, "uniform")])
 def test_fused_replay_verify(dev, B, Tp, T, d, acc_kind):
     """Replay of the previous window + verify of the next in one pass over the state:
     bit-identical to the two separate calls, and within tolerance of the oracle."""
